@@ -1,0 +1,95 @@
+"""Seeded synthetic inputs for the MXFP4 linear layer.
+
+Shared by the tests, the benchmark and the oracle checks.  It holds input
+recipes only -- shapes, distributions and seeds -- and none of the method's
+arithmetic (no quantization, no GEMM).
+
+The shapes are the six MXFP4 GEMM problems of the amd-mxfp4-mm leaderboard
+(the `PROFILE_TABLE` of submission 748756 and the benchmark table in the
+docstring of submission 733989).  The leaderboard's own input generator is not
+on the pages, so this recipe stands in for it: fp32 draws from numpy's PCG64
+generator (bit-identical across platforms), then rounded to bf16.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    seed: int
+    b_std: float = 1.0
+    outlier_frac: float = 0.0  # fraction of A entries multiplied by outlier_scale
+    outlier_scale: float = 100.0
+
+    @property
+    def label(self) -> str:
+        return f"M={self.M},N={self.N},K={self.K}"
+
+
+WORKLOADS: dict[str, Workload] = {
+    w.name: w
+    for w in (
+        Workload("m4_n2880_k512", 4, 2880, 512, seed=0),
+        Workload("m32_n4096_k512", 32, 4096, 512, seed=1),
+        Workload("m32_n2880_k512", 32, 2880, 512, seed=1),
+        Workload("m16_n2112_k7168", 16, 2112, 7168, seed=2, b_std=0.02, outlier_frac=0.01),
+        Workload("m64_n7168_k2048", 64, 7168, 2048, seed=3),
+        Workload("m256_n3072_k1536", 256, 3072, 1536, seed=4),
+    )
+}
+
+# The shape the headline latency is quoted on.
+HEADLINE = "m32_n4096_k512"
+
+
+def to_bf16(x: np.ndarray) -> torch.Tensor:
+    """fp32 numpy -> bf16 torch CPU tensor (round to nearest even)."""
+    return torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+
+
+def make_inputs(w: Workload | str) -> tuple[torch.Tensor, torch.Tensor]:
+    """(A bf16 [M, K], B bf16 [N, K]) on the CPU for a named workload.
+
+    Draw order: A ~ N(0, 1); then, if the workload has outliers, a uniform mask
+    selecting `outlier_frac` of A's entries, which are multiplied by
+    `outlier_scale`; then B ~ N(0, b_std^2)."""
+    if isinstance(w, str):
+        w = WORKLOADS[w]
+    return make_random(w.M, w.N, w.K, w.seed, b_std=w.b_std, outlier_frac=w.outlier_frac,
+                       outlier_scale=w.outlier_scale)
+
+
+def make_random(M: int, N: int, K: int, seed: int, b_std: float = 1.0, outlier_frac: float = 0.0,
+                outlier_scale: float = 100.0) -> tuple[torch.Tensor, torch.Tensor]:
+    rng = np.random.default_rng(seed)
+    a = rng.standard_normal((M, K), dtype=np.float32)
+    if outlier_frac > 0.0:
+        mask = rng.random((M, K)) < outlier_frac
+        a = np.where(mask, a * np.float32(outlier_scale), a).astype(np.float32)
+    b = rng.standard_normal((N, K), dtype=np.float32) * np.float32(b_std)
+    return to_bf16(a), to_bf16(b)
+
+
+def make_activation(M: int, K: int, seed: int, std: float = 1.0) -> torch.Tensor:
+    """A bf16 [M, K] ~ N(0, std^2)."""
+    rng = np.random.default_rng(seed)
+    return to_bf16(rng.standard_normal((M, K), dtype=np.float32) * np.float32(std))
+
+
+def all_bf16_patterns() -> torch.Tensor:
+    """Every finite bf16 bit pattern (NaN and +-inf excluded), as a 1-D bf16 tensor
+    whose length is a multiple of 32."""
+    u = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    exp = (u >> 7) & 0xFF
+    u = u[exp != 0xFF]
+    pad = (-u.size) % 32
+    u = np.concatenate([u, np.zeros(pad, np.uint16)])
+    return torch.from_numpy(u.view(np.int16).copy()).view(torch.bfloat16)
