@@ -1,0 +1,432 @@
+"""Benchmark of the MXFP4 linear layer (fused bf16 -> MXFP4 quantize + GEMM).
+
+One step = one call of the fused entry (mxfp4_quant_gemm) on one activation
+batch: A bf16 [M, K] quantized in-kernel, times a pre-packed MXFP4 weight
+[N, K], bf16 C [M, N] out.  The headline workload is M=32, N=4096, K=512.
+
+Timing: a CUDA graph of R calls, call i on copy i % R of both A and the packed
+weight, with R chosen so that the copies exceed twice the L2 cache (every call
+streams its operands from HBM); the graph is replayed until exactly K steps
+ran, bracketed by CUDA events on the replay stream.  Prints one JSON line.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "µs/call and % of roofline (HBM GB/s or FP4 TFLOPS) per MXFP4 GEMM shape"
+UNIT = "us/call"
+# The pages' published per-call time for the headline shape (MI355X, end to end
+# including Python dispatch; submission 733989's benchmark table).
+PAGES_US = {"m32_n4096_k512": 10.6, "m4_n2880_k512": 9.7, "m16_n2112_k7168": 20.9,
+            "m32_n2880_k512": 11.3, "m64_n7168_k2048": 17.5, "m256_n3072_k1536": 16.2}
+DENSE_FP4_TFLOPS_NOMINAL = 13500.0  # GB300 dense FP4 (no sparsity), nominal
+
+
+# ----------------------------------------------------------------------------- helpers
+def algorithmic_bytes(M: int, N: int, K: int, fused: bool = True) -> int:
+    """Each operand once: A (bf16 for the fused entry, codes+scales otherwise),
+    weight codes + scales, bf16 C."""
+    a = 2 * M * K if fused else M * K // 2 + M * K // 32
+    return a + N * K // 2 + N * K // 32 + 2 * M * N
+
+
+def flops(M: int, N: int, K: int) -> int:
+    return 2 * M * N * K
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_scaled_mxfp4_activation_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()[:16]
+
+
+def committed_traffic(workload: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary,
+    or None when the kernel source changed since it was captured."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    e = d.get(workload)
+    if not e or e.get("source_hash") != source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons while timing."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self) -> dict:
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------------- our arm
+class Problem:
+    """R rotating copies of A and of the packed weight for one workload."""
+
+    def __init__(self, w: workloads.Workload, device: torch.device, copies: int | None = None):
+        import block_scaled_mxfp4_activation_gb300 as mx
+
+        self.mx, self.w = mx, w
+        A, B = workloads.make_inputs(w)
+        W0 = mx.quantize_weights(B.to(device))
+        per_copy = W0.data.numel() + 2 * w.M * w.K + 2 * w.M * w.N
+        l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20))
+        self.copies = copies or max(2, math.ceil(2 * l2 / per_copy))
+        self.W = [W0] + [mx.PackedWeight(W0.data.clone(), w.N, w.K) for _ in range(self.copies - 1)]
+        A_dev = A.to(device)
+        self.A = [A_dev] + [A_dev.clone() for _ in range(self.copies - 1)]
+        self.C = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.copies)]
+        self.rotating_bytes = per_copy * self.copies
+        self.l2 = l2
+
+    def call(self, i: int):
+        j = i % self.copies
+        self.mx.quant_gemm(self.A[j], self.W[j], out=self.C[j])
+
+    def graph(self, n: int, stream: torch.cuda.Stream, rotate: bool = True) -> torch.cuda.CUDAGraph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(n):
+                    self.call(i if rotate else 0)
+        return g
+
+
+def time_graph_steps(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, rotate: bool = True,
+                     barrier=None):
+    """Exactly `steps` calls (graph replays), after `warmup` calls; returns ms."""
+    R = prob.copies if rotate else 1
+    chunk = min(steps, max(R, 256))
+    full, rest = divmod(steps, chunk)
+    g_full = prob.graph(chunk, stream, rotate)
+    g_rest = prob.graph(rest, stream, rotate) if rest else None
+    g_warm = prob.graph(max(warmup, 1), stream, rotate)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for _ in range(full):
+            g_full.replay()
+        if g_rest is not None:
+            g_rest.replay()
+        end.record(stream)
+    torch.cuda.synchronize()
+    if barrier:
+        barrier()
+    return start.elapsed_time(end)
+
+
+def time_e2e(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream) -> float:
+    """Per step: pinned host A -> device, the fused call through the public API,
+    device C -> pinned host.  Eager launches, no graph.  Returns ms."""
+    w = prob.w
+    hostA = prob.A[0].cpu().pin_memory()
+    hostC = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
+    devA = torch.empty_like(prob.A[0])
+    devC = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=devA.device)
+    mx = prob.mx
+
+    def step(i):
+        devA.copy_(hostA, non_blocking=True)
+        mx.quant_gemm(devA, prob.W[i % prob.copies], out=devC)
+        hostC.copy_(devC, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for i in range(warmup):
+            step(i)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        start.record(stream)
+        for i in range(steps):
+            step(i)
+        end.record(stream)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end)
+
+
+def shape_report(name: str, us: float, peaks: dict, fused: bool = True) -> dict:
+    w = workloads.WORKLOADS[name]
+    b = algorithmic_bytes(w.M, w.N, w.K, fused)
+    gbs = b / (us * 1e-6) / 1e9
+    tflops = flops(w.M, w.N, w.K) / (us * 1e-6) / 1e12
+    return {"us_per_call": round(us, 4), "bytes": b, "gbs": round(gbs, 1),
+            "hbm_frac": round(gbs / peaks["hbm_gbs"], 4), "fp4_tflops": round(tflops, 2),
+            "fp4_frac_nominal": round(tflops / DENSE_FP4_TFLOPS_NOMINAL, 5), "bound": "hbm"}
+
+
+def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
+    """The oracle (plain C, one thread, fp64) on a bounded sample of one call:
+    the whole activation is quantized, then a fixed set of output elements is
+    summed; the per-call time is scaled from the sampled elements to M*N."""
+    import oracle
+
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.make_inputs(w)
+    bq, bs = oracle.quantize(B)
+    rng = np.random.default_rng(0)
+    t0 = time.perf_counter()
+    aq, as_ = oracle.quantize(A)
+    t_quant = time.perf_counter() - t0
+    n_sample, spent, done = 256, 0.0, 0
+    while spent < budget_s:
+        ms = rng.integers(0, w.M, n_sample)
+        ns = rng.integers(0, w.N, n_sample)
+        t0 = time.perf_counter()
+        oracle.gemm_sampled(aq, as_, bq, bs, ms, ns)
+        spent += time.perf_counter() - t0
+        done += n_sample
+        n_sample = min(n_sample * 2, 1 << 16)
+    per_elem = spent / done
+    us = (t_quant + per_elem * w.M * w.N) * 1e6
+    return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{name}: full A quantization + {done} of {w.M * w.N} outputs (fp64, ascending k), "
+                      f"{spent:.1f} s, scaled to M*N"}
+
+
+def run_ours(args) -> dict:
+    import block_scaled_mxfp4_activation_gb300 as mx
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    barrier = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("gloo")
+        barrier = dist.barrier
+    mx.load_library()
+    peaks = measured_peaks()
+    stream = torch.cuda.Stream(device)
+    warmup = max(args.warmup, 3)
+
+    name = args.workload
+    w = workloads.WORKLOADS[name]
+    prob = Problem(w, device)
+    plan = mx.gemm_plan(w.M, w.N, w.K, fused=True)
+    assert mx.device_error(reset=True) == 0
+
+    with ClockSampler(local) as clk:
+        ms = time_graph_steps(prob, args.steps, warmup, stream, barrier=barrier)
+    clocks = clk.summary()
+    times = torch.tensor([ms], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_total = float(times[0])
+    us_call = ms_total * 1e3 / args.steps
+    value = us_call / world  # whole-job: world * steps calls in the max-over-ranks time
+
+    ms_warm = time_graph_steps(prob, min(args.steps, 2000), warmup, stream, rotate=False)
+    us_warm = ms_warm * 1e3 / min(args.steps, 2000)
+    e2e_steps = min(args.steps, 500)
+    ms_e2e = time_e2e(prob, e2e_steps, warmup, stream)
+    us_e2e = ms_e2e * 1e3 / e2e_steps
+    err = mx.device_error(reset=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x} after timing")
+
+    rep = shape_report(name, us_call, peaks)
+    traffic = committed_traffic(name)
+    out = {
+        "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": warmup, "ms_per_step": round(ms_total / args.steps, 7), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": round(value / PAGES_US[name], 4) if name in PAGES_US else None,
+        "vs_baseline_note": "pages' figure is end-to-end per call on MI355X incl. Python dispatch (context)",
+        "dtype": "mxfp4", "data": "synthetic",
+        "config": {"workload": f"{name}: fused bf16->MXFP4 quantize + block-scaled GEMM, {w.label}",
+                   "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
+                   "l2": f"{prob.copies} rotating copies of A and packed B ({prob.rotating_bytes / 2**20:.0f} MiB "
+                         f"> 2x L2 {prob.l2 / 2**20:.0f} MiB)",
+                   "timing": "CUDA graph of calls replayed, CUDA events on the replay stream",
+                   "plan": plan},
+        "roofline": {"bound": "hbm", "achieved": rep["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": rep["hbm_frac"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
+                     else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": rep["bytes"], "kernel": "mxfp4_gemm_kernel<fused>"},
+        "fp4": {"tflops": rep["fp4_tflops"], "frac_of_nominal_dense": rep["fp4_frac_nominal"]},
+        "warm_l2_us_per_call": round(us_warm, 4),
+        "e2e": {"value": round(us_e2e, 3), "unit": UNIT, "h2d_bytes_per_step": 2 * w.M * w.K,
+                "d2h_bytes_per_step": 2 * w.M * w.N,
+                "how": "pinned A -> device, mx.quant_gemm (C ABI), C -> pinned host; eager, per step"},
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    if args.all_shapes:
+        shapes = {}
+        for other in workloads.WORKLOADS:
+            wo = workloads.WORKLOADS[other]
+            p = prob if other == name else Problem(wo, device)
+            n = min(max(args.steps, 1000), 4000)
+            t = time_graph_steps(p, n, warmup, stream)
+            r = shape_report(other, t * 1e3 / n, peaks)
+            r["plan"] = mx.gemm_plan(wo.M, wo.N, wo.K, fused=True)
+            r["pages_us_mi355x"] = PAGES_US.get(other)
+            shapes[other] = r
+            if p is not prob:
+                del p
+                torch.cuda.empty_cache()
+        out["per_shape"] = shapes
+    if rank == 0 and world == 1 and not args.no_cpu:
+        out["cpu_baseline"] = cpu_baseline(name)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return out if rank == 0 else None
+
+
+# ----------------------------------------------------------------------------- reference arm
+def run_reference(args) -> dict | None:
+    """The oracle timed on the host cores, on a bounded sample per step."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    import oracle
+
+    oracle.build()
+    name = args.workload
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.make_inputs(w)
+    bq, bs = oracle.quantize(B)
+    warmup = max(args.warmup, 3)
+    per_step_budget = max(0.05, min(2.0, 150.0 / (args.steps + warmup)))
+    # calibrate the sample size of one step
+    aq, as_ = oracle.quantize(A)
+    rng = np.random.default_rng(1)
+    t0 = time.perf_counter()
+    oracle.gemm_sampled(aq, as_, bq, bs, rng.integers(0, w.M, 64), rng.integers(0, w.N, 64))
+    per_elem = (time.perf_counter() - t0) / 64
+    n_sample = int(max(16, min(w.M * w.N, per_step_budget / per_elem)))
+    times = []
+    for i in range(warmup + args.steps):
+        ms = rng.integers(0, w.M, n_sample)
+        ns = rng.integers(0, w.N, n_sample)
+        t0 = time.perf_counter()
+        aq, as_ = oracle.quantize(A)
+        tq = time.perf_counter() - t0
+        t1 = time.perf_counter()
+        oracle.gemm_sampled(aq, as_, bq, bs, ms, ns)
+        tg = time.perf_counter() - t1
+        if i >= warmup:
+            times.append((tq + tg * (w.M * w.N) / n_sample) * 1e6)
+    us = float(np.mean(times))
+    sample = f"{name}: per step, full A quantization + {n_sample} of {w.M * w.N} outputs, scaled to M*N"
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": warmup, "ms_per_step": round(us / 1e3, 4), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{name}: fused bf16->MXFP4 quantize + GEMM, {w.label}", "M": w.M, "N": w.N,
+                   "K": w.K, "seed": w.seed},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--all-shapes", dest="all_shapes", action="store_true", default=True)
+    ap.add_argument("--headline-only", dest="all_shapes", action="store_false")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    args = ap.parse_args(argv)
+    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if out is not None:
+        print(json.dumps(out), flush=True)
+
+
+if __name__ == "__main__":
+    main()

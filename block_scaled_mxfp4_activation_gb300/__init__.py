@@ -1,0 +1,264 @@
+"""MXFP4 linear layer on one GB300: a thin ctypes binding over libmxfp4.so.
+
+Every call marshals torch tensors into the C ABI declared in
+``include/mxfp4.h`` and launches the library's CUDA kernels on the current
+torch stream; torch provides device memory and streams only.  There is no
+fallback: if the library cannot be loaded, or a call fails, an exception is
+raised.
+
+    C[M, N] = A[M, K] @ B[N, K]^T,  A bf16 quantized on the fly to MXFP4,
+    B pre-quantized MXFP4 (E2M1 codes + one E8M0 scale per 32 K elements).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from dataclasses import dataclass
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "MXFP4Error", "PackedWeight", "load_library", "library_path", "quantize", "packed_weight_bytes",
+    "pack_weights", "unpack_weights", "quantize_weights", "gemm", "quant_gemm", "gemm_plan",
+    "gemm_with_plan", "workspace_bytes", "device_error", "set_wait_timeout_ns", "diag_wait_timeout",
+    "status_string", "Plan",
+]
+
+MXFP4_OK = 0
+MXFP4_ERR_DEVICE_TIMEOUT = 6
+STATUS_NAMES = {
+    0: "MXFP4_OK", 1: "MXFP4_ERR_INVALID_ARG", 2: "MXFP4_ERR_UNSUPPORTED_SHAPE",
+    3: "MXFP4_ERR_MISALIGNED", 4: "MXFP4_ERR_WORKSPACE_TOO_SMALL", 5: "MXFP4_ERR_CUDA",
+    6: "MXFP4_ERR_DEVICE_TIMEOUT", 7: "MXFP4_ERR_UNSUPPORTED_DEVICE",
+}
+
+
+class MXFP4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+
+
+class Plan(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "block_m", "splits", "stages", "k_tiles_per_split", "grid_x", "grid_y", "grid_z", "threads",
+        "smem_bytes", "tmem_cols")]
+
+    def as_dict(self) -> dict:
+        return {n: getattr(self, n) for n, _ in self._fields_}
+
+
+_lib = None
+_lock = threading.Lock()
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
+    """Load libmxfp4.so (compiling it with nvcc first if it is missing or stale)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = _build.build() if build_if_missing else _build.LIB
+        if not os.path.exists(path):
+            raise RuntimeError(f"libmxfp4.so not found at {path}; run build() first")
+        lib = ctypes.CDLL(path)
+        P, I, S, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+        st = ctypes.c_int
+        sig = {
+            "mxfp4_quantize": ([P, I, I, I, P, P, S], st),
+            "mxfp4_packed_weight_bytes": ([I, I], Z),
+            "mxfp4_pack_weights": ([P, P, I, I, P, S], st),
+            "mxfp4_unpack_weights": ([P, I, I, P, P, S], st),
+            "mxfp4_workspace_bytes": ([I, I, I], Z),
+            "mxfp4_gemm": ([P, P, P, P, I, I, I, P, Z, S], st),
+            "mxfp4_quant_gemm": ([P, I, P, P, I, I, I, P, Z, S], st),
+            "mxfp4_gemm_plan": ([I, I, I, ctypes.c_int, ctypes.POINTER(Plan)], st),
+            "mxfp4_gemm_with_plan": ([P, I, P, P, P, I, I, I, ctypes.c_int, ctypes.POINTER(Plan), S], st),
+            "mxfp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
+            "mxfp4_device_error": ([S, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], st),
+            "mxfp4_set_wait_timeout_ns": ([ctypes.c_uint64], st),
+            "mxfp4_diag_wait_timeout": ([S], st),
+        }
+        for name, (args, res) in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = res
+        _lib = lib
+        return lib
+
+
+def status_string(status: int) -> str:
+    try:
+        return load_library().mxfp4_status_string(int(status)).decode()
+    except Exception:  # the message must not hide the original failure
+        return "?"
+
+
+def _stream(stream=None) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return int(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor | None):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _call(name: str, *args):
+    status = getattr(load_library(), name)(*args)
+    if status != MXFP4_OK:
+        raise MXFP4Error(status, name)
+
+
+def _need(t: torch.Tensor, dtype: torch.dtype, what: str):
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda:
+        raise TypeError(f"{what} must be a CUDA {dtype} tensor")
+
+
+# ----------------------------------------------------------------------------- quantization
+def quantize(A: torch.Tensor, out: tuple[torch.Tensor, torch.Tensor] | None = None, stream=None):
+    """bf16 A [M, K] (row stride = lda) -> (codes uint8 [M, K/2], scales uint8 [M, K/32])."""
+    _need(A, torch.bfloat16, "A")
+    if A.dim() != 2 or A.stride(1) != 1:
+        raise ValueError("A must be 2-D with unit column stride")
+    M, K = A.shape
+    if out is None:
+        out = (torch.empty((M, K // 2), dtype=torch.uint8, device=A.device),
+               torch.empty((M, K // 32), dtype=torch.uint8, device=A.device))
+    Aq, As = out
+    _call("mxfp4_quantize", _ptr(A), M, K, A.stride(0), _ptr(Aq), _ptr(As), _stream(stream))
+    return Aq, As
+
+
+def packed_weight_bytes(N: int, K: int) -> int:
+    n = load_library().mxfp4_packed_weight_bytes(N, K)
+    if n == 0:
+        raise MXFP4Error(1, "mxfp4_packed_weight_bytes")
+    return n
+
+
+def pack_weights(Bq: torch.Tensor, Bs: torch.Tensor, out: torch.Tensor | None = None, stream=None):
+    """Natural (codes [N, K/2], scales [N, K/32]) -> the packed weight buffer."""
+    _need(Bq, torch.uint8, "Bq")
+    _need(Bs, torch.uint8, "Bs")
+    N, K = Bq.shape[0], Bq.shape[1] * 2
+    if not (Bq.is_contiguous() and Bs.is_contiguous() and Bs.shape == (N, K // 32)):
+        raise ValueError("Bq [N, K/2] and Bs [N, K/32] must be contiguous")
+    if out is None:
+        out = torch.empty(packed_weight_bytes(N, K), dtype=torch.uint8, device=Bq.device)
+    _call("mxfp4_pack_weights", _ptr(Bq), _ptr(Bs), N, K, _ptr(out), _stream(stream))
+    return out
+
+
+def unpack_weights(Bp: torch.Tensor, N: int, K: int, stream=None):
+    """Packed weight buffer -> (codes [N, K/2], scales [N, K/32])."""
+    _need(Bp, torch.uint8, "Bp")
+    Bq = torch.empty((N, K // 2), dtype=torch.uint8, device=Bp.device)
+    Bs = torch.empty((N, K // 32), dtype=torch.uint8, device=Bp.device)
+    _call("mxfp4_unpack_weights", _ptr(Bp), N, K, _ptr(Bq), _ptr(Bs), _stream(stream))
+    return Bq, Bs
+
+
+@dataclass
+class PackedWeight:
+    """A weight matrix B [N, K] quantized to MXFP4 and packed for the GEMM."""
+    data: torch.Tensor
+    N: int
+    K: int
+
+
+def quantize_weights(B: torch.Tensor, stream=None) -> PackedWeight:
+    """bf16 B [N, K] -> PackedWeight (quantized with the activation rule, then packed)."""
+    Bq, Bs = quantize(B, stream=stream)
+    return PackedWeight(pack_weights(Bq, Bs, stream=stream), B.shape[0], B.shape[1])
+
+
+# ----------------------------------------------------------------------------- GEMM
+def workspace_bytes(M: int, N: int, K: int) -> int:
+    return int(load_library().mxfp4_workspace_bytes(M, N, K))
+
+
+def _weight(W: PackedWeight) -> PackedWeight:
+    if not isinstance(W, PackedWeight):
+        raise TypeError("weights must be a PackedWeight (see quantize_weights / pack_weights)")
+    return W
+
+
+def gemm(Aq: torch.Tensor, As: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """Pre-quantized A (codes [M, K/2], scales [M, K/32]) x packed W -> bf16 C [M, N]."""
+    W = _weight(W)
+    _need(Aq, torch.uint8, "Aq")
+    _need(As, torch.uint8, "As")
+    M = Aq.shape[0]
+    if Aq.shape != (M, W.K // 2) or As.shape != (M, W.K // 32) or not (Aq.is_contiguous() and As.is_contiguous()):
+        raise ValueError("Aq/As shapes do not match the weight's K")
+    if out is None:
+        out = torch.empty((M, W.N), dtype=torch.bfloat16, device=Aq.device)
+    _call("mxfp4_gemm", _ptr(Aq), _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K, None, 0, _stream(stream))
+    return out
+
+
+def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The fused layer: bf16 A [M, K] -> quantize in-kernel -> x packed W -> bf16 C [M, N]."""
+    W = _weight(W)
+    _need(A, torch.bfloat16, "A")
+    if A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+        raise ValueError("A must be [M, K] with unit column stride")
+    M = A.shape[0]
+    if out is None:
+        out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
+    _call("mxfp4_quant_gemm", _ptr(A), A.stride(0), _ptr(W.data), _ptr(out), M, W.N, W.K, None, 0,
+          _stream(stream))
+    return out
+
+
+def gemm_plan(M: int, N: int, K: int, fused: bool = True) -> dict:
+    p = Plan()
+    _call("mxfp4_gemm_plan", M, N, K, int(fused), ctypes.byref(p))
+    return p.as_dict()
+
+
+def gemm_with_plan(A_or_Aq: torch.Tensor, As: torch.Tensor | None, W: PackedWeight, plan: dict,
+                   fused: bool, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Either GEMM entry with an explicit tile plan (block_m, splits, stages)."""
+    W = _weight(W)
+    M = A_or_Aq.shape[0]
+    if fused:
+        _need(A_or_Aq, torch.bfloat16, "A")
+        lda = A_or_Aq.stride(0)
+    else:
+        _need(A_or_Aq, torch.uint8, "Aq")
+        _need(As, torch.uint8, "As")
+        lda = W.K // 2
+    if out is None:
+        out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A_or_Aq.device)
+    p = Plan()
+    p.block_m, p.splits, p.stages = int(plan["block_m"]), int(plan["splits"]), int(plan.get("stages", 0))
+    _call("mxfp4_gemm_with_plan", _ptr(A_or_Aq), lda, _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K,
+          int(fused), ctypes.byref(p), _stream(stream))
+    return out
+
+
+# ----------------------------------------------------------------------------- diagnostics
+def device_error(reset: bool = True, stream=None) -> int:
+    """Synchronise the stream and return the device error word (0 = none)."""
+    code = ctypes.c_uint32(0)
+    status = load_library().mxfp4_device_error(_stream(stream), int(reset), ctypes.byref(code))
+    if status not in (MXFP4_OK, MXFP4_ERR_DEVICE_TIMEOUT):
+        raise MXFP4Error(status, "mxfp4_device_error")
+    return int(code.value)
+
+
+def set_wait_timeout_ns(ns: int) -> None:
+    _call("mxfp4_set_wait_timeout_ns", int(ns))
+
+
+def diag_wait_timeout(stream=None) -> None:
+    _call("mxfp4_diag_wait_timeout", _stream(stream))

@@ -1,0 +1,258 @@
+// The C ABI: argument checks, device checks, tensor-map encoding, plan choice
+// and launches.  Nothing here allocates device memory.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <mutex>
+
+#include "internal.h"
+
+namespace mxfp4 {
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  bool ok = false;
+  cudaDeviceProp prop{};
+};
+
+// Properties of the current device, cached per device; ok only on sm_103.
+const DeviceInfo* current_device(mxfp4_status_t* st) {
+  static DeviceInfo info[64];
+  static std::once_flag once[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = MXFP4_ERR_CUDA;
+    return nullptr;
+  }
+  std::call_once(once[dev], [dev]() {
+    if (cudaGetDeviceProperties(&info[dev].prop, dev) == cudaSuccess)
+      info[dev].ok = info[dev].prop.major == 10 && info[dev].prop.minor == 3;
+  });
+  if (!info[dev].ok) {
+    *st = MXFP4_ERR_UNSUPPORTED_DEVICE;
+    return nullptr;
+  }
+  *st = MXFP4_OK;
+  return &info[dev];
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, []() {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D map over the packed weight codes [n_pad, K/2] bytes: 128 x 128-byte
+// boxes, 128-byte swizzle (the canonical K-major layout the MMA descriptor
+// reads); columns past K/2 read as zero.
+bool encode_weight_map(const void* bpacked, int64_t N, int64_t K, CUtensorMap* map) {
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return false;
+  const PackedLayout L = packed_layout(N, K);
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(L.n_pad)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKBytes), static_cast<cuuint32_t>(kTileN)};
+  cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(bpacked), dims, strides,
+                            box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
+mxfp4_status_t check_mnk(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  // 32-bit indices inside the kernels
+  if (M * N > (int64_t(1) << 31) || K / 2 * ceil_div(N, kTileN) * kTileN > (int64_t(1) << 40))
+    return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  return MXFP4_OK;
+}
+
+mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* bpacked, void* C,
+                        int64_t M, int64_t N, int64_t K, bool fused, const mxfp4_plan_t* user_plan,
+                        cudaStream_t stream) {
+  mxfp4_status_t st = check_mnk(M, N, K);
+  if (st != MXFP4_OK) return st;
+  if (a == nullptr || bpacked == nullptr || C == nullptr || (!fused && as == nullptr))
+    return MXFP4_ERR_INVALID_ARG;
+  if (fused && lda < K) return MXFP4_ERR_INVALID_ARG;
+  if (!aligned16(a) || !aligned16(bpacked) || !aligned16(C) || (fused && lda % 8 != 0))
+    return MXFP4_ERR_MISALIGNED;
+  if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  const DeviceInfo* dev = current_device(&st);
+  if (dev == nullptr) return st;
+  mxfp4_plan_t plan;
+  if (user_plan != nullptr) {
+    plan = mxfp4_plan_t{};
+    plan.block_m = user_plan->block_m;
+    plan.splits = user_plan->splits;
+    plan.stages = user_plan->stages;
+    if (!finish_plan(M, N, K, fused, dev->prop, &plan)) return MXFP4_ERR_INVALID_ARG;
+  } else {
+    default_plan(M, N, K, fused, dev->prop, &plan);
+    if (plan.threads == 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  }
+  CUtensorMap map;
+  if (!encode_weight_map(bpacked, N, K, &map)) return MXFP4_ERR_CUDA;
+  GemmArgs g{};
+  g.a = a;
+  g.a_scales = static_cast<const uint8_t*>(as);
+  const PackedLayout L = packed_layout(N, K);
+  g.b_sf = static_cast<const uint8_t*>(bpacked) + L.sf_offset;
+  g.c = static_cast<__nv_bfloat16*>(C);
+  g.M = static_cast<int32_t>(M);
+  g.N = static_cast<int32_t>(N);
+  g.K = static_cast<int32_t>(K);
+  g.lda = fused ? lda : K / 2;
+  g.k_tiles = static_cast<int32_t>(L.k_tiles);
+  g.kt_per_split = plan.k_tiles_per_split;
+  g.splits = plan.splits;
+  g.stages = plan.stages;
+  g.tmem_cols = static_cast<uint32_t>(plan.tmem_cols);
+  g.timeout_ns = g_timeout_ns.load();
+  g.err = device_error_word();
+  if (g.err == nullptr) return MXFP4_ERR_CUDA;
+  return launch_gemm(map, g, plan, fused, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace mxfp4
+
+using namespace mxfp4;
+
+extern "C" {
+
+mxfp4_status_t mxfp4_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
+                              mxfp4_stream_t stream) {
+  if (A == nullptr || Aq == nullptr || As == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (M < 1 || K < 32 || K % 32 != 0 || lda < K) return MXFP4_ERR_INVALID_ARG;
+  if (M > kMaxDim || K > kMaxDim || M * (K / 8) > (int64_t(1) << 31) * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(Aq) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  mxfp4_status_t st;
+  if (current_device(&st) == nullptr) return st;
+  return launch_quantize(A, M, K, lda, Aq, As, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP4_OK
+             : MXFP4_ERR_CUDA;
+}
+
+size_t mxfp4_packed_weight_bytes(int64_t N, int64_t K) {
+  if (N < 1 || K < 32 || K % 32 != 0 || N > kMaxDim || K > kMaxDim) return 0;
+  return packed_layout(N, K).total;
+}
+
+mxfp4_status_t mxfp4_pack_weights(const void* Bq, const void* Bs, int64_t N, int64_t K, void* Bpacked,
+                                  mxfp4_stream_t stream) {
+  if (Bq == nullptr || Bs == nullptr || Bpacked == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (N < 1 || K < 32 || K % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (N > kMaxDim || K > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(Bq) || !aligned16(Bpacked)) return MXFP4_ERR_MISALIGNED;
+  mxfp4_status_t st;
+  if (current_device(&st) == nullptr) return st;
+  return launch_pack_weights(Bq, Bs, N, K, Bpacked, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP4_OK
+             : MXFP4_ERR_CUDA;
+}
+
+mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, void* Bq, void* Bs,
+                                    mxfp4_stream_t stream) {
+  if (Bq == nullptr || Bs == nullptr || Bpacked == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (N < 1 || K < 32 || K % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (N > kMaxDim || K > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(Bq) || !aligned16(Bpacked)) return MXFP4_ERR_MISALIGNED;
+  mxfp4_status_t st;
+  if (current_device(&st) == nullptr) return st;
+  return launch_unpack_weights(Bpacked, N, K, Bq, Bs, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP4_OK
+             : MXFP4_ERR_CUDA;
+}
+
+size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+  (void)M;
+  (void)N;
+  (void)K;
+  return 0;  // K splits are reduced on chip, through cluster shared memory
+}
+
+mxfp4_status_t mxfp4_gemm(const void* Aq, const void* As, const void* Bpacked, void* C, int64_t M,
+                          int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+  (void)ws;
+  if (ws_bytes < mxfp4_workspace_bytes(M, N, K)) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+  return run_gemm(Aq, K / 2, As, Bpacked, C, M, N, K, false, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M,
+                                int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+  (void)ws;
+  if (ws_bytes < mxfp4_workspace_bytes(M, N, K)) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+  return run_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, reinterpret_cast<cudaStream_t>(stream));
+}
+
+mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan) {
+  if (plan == nullptr) return MXFP4_ERR_INVALID_ARG;
+  mxfp4_status_t st = check_mnk(M, N, K);
+  if (st != MXFP4_OK) return st;
+  const DeviceInfo* dev = current_device(&st);
+  if (dev == nullptr) return st;
+  default_plan(M, N, K, fused != 0, dev->prop, plan);
+  return plan->threads == 0 ? MXFP4_ERR_UNSUPPORTED_SHAPE : MXFP4_OK;
+}
+
+mxfp4_status_t mxfp4_gemm_with_plan(const void* A_or_Aq, int64_t lda, const void* As, const void* Bpacked,
+                                    void* C, int64_t M, int64_t N, int64_t K, int fused,
+                                    const mxfp4_plan_t* plan, mxfp4_stream_t stream) {
+  if (plan == nullptr) return MXFP4_ERR_INVALID_ARG;
+  return run_gemm(A_or_Aq, fused ? lda : K / 2, As, Bpacked, C, M, N, K, fused != 0, plan,
+                  reinterpret_cast<cudaStream_t>(stream));
+}
+
+const char* mxfp4_status_string(mxfp4_status_t status) {
+  switch (status) {
+    case MXFP4_OK: return "ok";
+    case MXFP4_ERR_INVALID_ARG: return "invalid argument";
+    case MXFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MXFP4_ERR_MISALIGNED: return "pointer or leading dimension not 16-byte aligned";
+    case MXFP4_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MXFP4_ERR_CUDA: return "CUDA error";
+    case MXFP4_ERR_DEVICE_TIMEOUT: return "a device-side wait timed out";
+    case MXFP4_ERR_UNSUPPORTED_DEVICE: return "current device is not sm_103 (GB300)";
+  }
+  return "unknown status";
+}
+
+mxfp4_status_t mxfp4_device_error(mxfp4_stream_t stream, int reset, uint32_t* code) {
+  if (code == nullptr) return MXFP4_ERR_INVALID_ARG;
+  mxfp4_status_t st;
+  if (current_device(&st) == nullptr) return st;
+  if (read_device_error(reinterpret_cast<cudaStream_t>(stream), code, reset != 0) != cudaSuccess)
+    return MXFP4_ERR_CUDA;
+  return *code != 0 ? MXFP4_ERR_DEVICE_TIMEOUT : MXFP4_OK;
+}
+
+mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns) {
+  g_timeout_ns.store(ns == 0 ? 1000000000ull : ns);
+  return MXFP4_OK;
+}
+
+mxfp4_status_t mxfp4_diag_wait_timeout(mxfp4_stream_t stream) {
+  mxfp4_status_t st;
+  if (current_device(&st) == nullptr) return st;
+  return launch_diag_wait(g_timeout_ns.load(), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MXFP4_OK
+             : MXFP4_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,463 @@
+// Block-scaled MXFP4 GEMM on the 5th-generation tensor cores (tcgen05,
+// kind::mxf4, UE8M0 scales), with the activation quantized in the kernel
+// (fused entry) or read pre-quantized.
+//
+// The pages' kernels (`kernel_fused_mxfp4_gemm` of submission 748756,
+// `_tiled_gemm_engine` of submission 754569, the fused split-K kernels of
+// submission 755056) quantize a bf16 A tile in registers, load packed FP4 B
+// and its scales, and call `tl.dot_scaled` per K tile, with split-K partials
+// reduced by a second kernel.  Here, per CTA:
+//
+//   - the output tile is C^T[128 weight rows, block_m activation rows]: the
+//     weights are the MMA's A operand (M = 128) and the activations its B
+//     operand (N = block_m), so a handful of tokens still fills the MMA;
+//   - warp 0 streams 128 x 256 tiles of packed weight codes with TMA (128-byte
+//     swizzle) plus their 1 KB of pre-arranged scales with a bulk copy;
+//   - warps 2.. quantize the bf16 activation tile straight into shared memory,
+//     in the operand's swizzled layout, and write its scales in the
+//     tensor-memory scale-chunk layout;
+//   - warp 1 moves both scale sets to tensor memory (tcgen05.cp) and issues
+//     four K = 64 block-scaled MMAs per stage into an fp32 accumulator in
+//     tensor memory;
+//   - K splits of one output tile form a thread-block cluster: each CTA
+//     stages its fp32 partial tile in shared memory and the cluster sums the
+//     partials through distributed shared memory in a fixed order
+//     (deterministic, no global workspace, no second kernel);
+//   - bf16 is written with 8-byte coalesced stores.
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace mxfp4 {
+
+template <int BM>
+struct TileCfg {
+  static constexpr int kRowChunks = BM > 128 ? 2 : 1;             // 128-row scale chunks of A
+  static constexpr int kBTileBytes = kTileN * kTileKBytes;         // 16 KB of weight codes
+  static constexpr int kATileBytes = BM * kTileKBytes;             // activation codes
+  static constexpr int kSfaStageBytes = 2 * kRowChunks * kSfChunkBytes;
+  static constexpr int kStageBytes = kBTileBytes + kATileBytes + kSfTileBytes + kSfaStageBytes;
+  static constexpr int kAWarps = BM >= 128 ? 8 : 4;                // producer / epilogue warps
+  static constexpr int kAThreads = kAWarps * 32;
+  static constexpr int kThreads = 64 + kAThreads;
+  static constexpr int kSfCols = 8 + 8 * kRowChunks;               // TMEM scale columns per stage
+  static constexpr int kStagingBytes = BM * kTileN * 4;            // fp32 partial tile
+  static_assert(BM % 32 == 0 && BM <= 256, "block_m must be 32, 64, 128 or 256");
+};
+
+// Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 scales, fp32
+// accumulate): A/B formats at bits 7-9 / 10-12 (E2M1 = 1), both K-major, N >> 3
+// at bits 17-22, scale type UE8M0 at bit 23, M >> 4 at bits 24-28; the byte of
+// each scale word used by this MMA (0 or 2: scales 0-1 or 2-3 of a 4-scale
+// chunk) at bits 29-30 (A) and 4-5 (B).
+template <int BM>
+__device__ __forceinline__ uint32_t mxf4_idesc(uint32_t scale_id) {
+  return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BM >> 3) << 17) | (1u << 23) |
+         (static_cast<uint32_t>(kTileN >> 4) << 24) | (scale_id << 29) | (scale_id << 4);
+}
+
+// Shared-memory layout of one CTA (offsets from a 1024-byte aligned base).
+struct SmemLayout {
+  uint32_t a_off, sfw_off, sfa_off, bar_off, total;
+};
+
+template <int BM>
+__host__ __device__ inline SmemLayout smem_layout(int stages) {
+  using C = TileCfg<BM>;
+  SmemLayout L;
+  L.a_off = stages * C::kBTileBytes;
+  L.sfw_off = L.a_off + stages * C::kATileBytes;
+  L.sfa_off = L.sfw_off + stages * kSfTileBytes;
+  const uint32_t end = L.sfa_off + stages * C::kSfaStageBytes;
+  L.bar_off = end > static_cast<uint32_t>(C::kStagingBytes) ? end : C::kStagingBytes;
+  // barriers: full_tma[stages], full_a[stages], empty[stages], accum; then the
+  // tensor-memory address and the abort flag
+  L.total = L.bar_off + (3 * stages + 1) * 8 + 16;
+  return L;
+}
+
+template <int BM, bool kFused>
+__global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
+    mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+  using C = TileCfg<BM>;
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const uint32_t sbase = smem_u32(smem);
+  const int stages = args.stages;
+  const SmemLayout L = smem_layout<BM>(stages);
+  auto full_tma = [&](int s) { return sbase + L.bar_off + 8u * s; };
+  auto full_a = [&](int s) { return sbase + L.bar_off + 8u * (stages + s); };
+  auto empty = [&](int s) { return sbase + L.bar_off + 8u * (2 * stages + s); };
+  const uint32_t accum_bar = sbase + L.bar_off + 8u * (3 * stages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.bar_off + 8 * (3 * stages + 1));
+  volatile uint32_t* abort_flag = tmem_slot + 1;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int splits = args.splits;
+  const uint32_t rank = splits > 1 ? cluster_ctarank() : 0u;
+  const int n_tile = blockIdx.y, m_tile = blockIdx.z;
+  const int kt_begin = static_cast<int>(rank) * args.kt_per_split;
+  const int kt_end = min(args.k_tiles, kt_begin + args.kt_per_split);
+  const int kt_count = max(0, kt_end - kt_begin);
+  const uint64_t timeout = args.timeout_ns;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < stages; ++s) {
+      mbar_init(full_tma(s), 1);
+      mbar_init(full_a(s), C::kAThreads);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(accum_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_b);
+  if (warp == 1) {
+    tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
+    tmem_relinquish();
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  const uint32_t tmem_sf = tmem_base + BM;  // scale columns follow the accumulator
+
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      const uint64_t policy = policy_evict_first();  // weights are read once per call
+      int issued = 0;
+      for (int i = 0; i < kt_count; ++i) {
+        const int s = i % stages, round = i / stages;
+        if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+          report_error(args.err, kErrWaitEmpty);
+          *abort_flag = 1u;
+        }
+        if (*abort_flag) break;
+        const int kt = kt_begin + i;
+        mbar_arrive_expect_tx(full_tma(s), C::kBTileBytes + kSfTileBytes);
+        tma_load_2d(sbase + s * C::kBTileBytes, &tmap_b, kt * kTileKBytes, n_tile * kTileN, full_tma(s),
+                    policy);
+        bulk_load(sbase + L.sfw_off + s * kSfTileBytes,
+                  args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes,
+                  kSfTileBytes, full_tma(s), policy);
+        issued = i + 1;
+      }
+      // Before the CTA can exit, every copy it issued must have landed.
+      for (int s = 0; s < stages && s < issued; ++s) {
+        const int last = s + stages * ((issued - 1 - s) / stages);
+        if (!mbar_wait(full_tma(s), (last / stages) & 1, timeout)) report_error(args.err, kErrWaitDrain);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ------------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      for (int i = 0; i < kt_count; ++i) {
+        const int s = i % stages, round = i / stages;
+        bool ok = mbar_wait(full_tma(s), round & 1, timeout);
+        if (!ok) report_error(args.err, kErrWaitTma);
+        ok = ok && mbar_wait(full_a(s), round & 1, timeout);
+        if (!ok) {
+          report_error(args.err, kErrWaitA);
+          *abort_flag = 1u;
+        }
+        if (*abort_flag) break;
+        tc_fence_after_sync();
+        const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
+        const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
+        const uint32_t sfw_s = sbase + L.sfw_off + s * kSfTileBytes;
+        const uint32_t sfa_s = sbase + L.sfa_off + s * C::kSfaStageBytes;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) tmem_cp_32x128b_warpx4(sfw_t + 4 * c, smem_desc(sfw_s + c * kSfChunkBytes, 128, 128, 0));
+#pragma unroll
+        for (int c = 0; c < 2 * C::kRowChunks; ++c)
+          tmem_cp_32x128b_warpx4(sfa_t + 4 * c, smem_desc(sfa_s + c * kSfChunkBytes, 128, 128, 0));
+        const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
+        const uint64_t b_desc = smem_desc(sbase + L.a_off + s * C::kATileBytes, 16, 1024, 2);
+        const int k0 = (kt_begin + i) * kTileK;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          if (k0 + 64 * j >= args.K) break;
+          const uint32_t sid = (j & 1) * 2;
+          // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 -> +2)
+          mma_mxf4(tmem_base, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>(sid), sfw_t + 4 * (j >> 1),
+                   sfa_t + 4 * C::kRowChunks * (j >> 1), (i | j) != 0);
+        }
+        if (i + stages < kt_count) tc_commit(empty(s));  // frees the stage when these MMAs finish
+      }
+      tc_commit(accum_bar);  // always: the epilogue waits on it
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------------ activation producer
+    const int tid = threadIdx.x - 64;
+    const int m_base = m_tile * BM;
+    for (int i = 0; i < kt_count; ++i) {
+      const int s = i % stages, round = i / stages;
+      if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+        report_error(args.err, kErrWaitEmpty);
+        *abort_flag = 1u;
+      }
+      if (*abort_flag) break;
+      const int k0 = (kt_begin + i) * kTileK;
+      uint8_t* a_tile = smem + L.a_off + s * C::kATileBytes;
+      uint8_t* sfa = smem + L.sfa_off + s * C::kSfaStageBytes;
+      if constexpr (kFused) {
+        // 16-byte units: 32 per row of the tile (256 bf16), lanes 4b..4b+3 = block b
+        constexpr int kUnits = BM * 32 / C::kAThreads;
+        constexpr int kBatch = kUnits < 8 ? kUnits : 8;
+        const uint16_t* A = static_cast<const uint16_t*>(args.a);
+#pragma unroll
+        for (int t0 = 0; t0 < kUnits; t0 += kBatch) {
+          uint4 v[kBatch];
+#pragma unroll
+          for (int t = 0; t < kBatch; ++t) {
+            const int u = tid + (t0 + t) * C::kAThreads;
+            const int m = u >> 5, j = u & 31;
+            const int gm = m_base + m, gk = k0 + j * 8;
+            v[t] = make_uint4(0, 0, 0, 0);
+            if (gm < args.M && gk < args.K)
+              v[t] = __ldg(reinterpret_cast<const uint4*>(A + static_cast<int64_t>(gm) * args.lda + gk));
+          }
+#pragma unroll
+          for (int t = 0; t < kBatch; ++t) {
+            const int u = tid + (t0 + t) * C::kAThreads;
+            const int m = u >> 5, j = u & 31, b = j >> 2, q = j & 3;
+            uint32_t byte;
+            const uint32_t codes = quantize_quad(v[t], &byte);
+            *reinterpret_cast<uint32_t*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + q * 4) = codes;
+            if (q == 0) {
+              const int r = m & 127;
+              sfa[((b >> 2) * C::kRowChunks + (m >> 7)) * kSfChunkBytes + (r & 31) * 16 + (r >> 5) * 4 + (b & 3)] =
+                  static_cast<uint8_t>(byte);
+            }
+          }
+        }
+      } else {
+        // 16-byte units = one 32-element block of codes: 8 per row of the tile
+        constexpr int kUnits = BM * 8 / C::kAThreads;
+        const uint8_t* Aq = static_cast<const uint8_t*>(args.a);
+        const int64_t kh = args.K / 2, nblk = args.K / 32;
+        uint4 v[kUnits];
+        uint8_t sc[kUnits];
+#pragma unroll
+        for (int t = 0; t < kUnits; ++t) {
+          const int u = tid + t * C::kAThreads;
+          const int m = u >> 3, b = u & 7;
+          const int gm = m_base + m, gk = k0 + b * 32;
+          v[t] = make_uint4(0, 0, 0, 0);
+          sc[t] = 0;
+          if (gm < args.M && gk < args.K) {
+            v[t] = __ldg(reinterpret_cast<const uint4*>(Aq + gm * kh + gk / 2));
+            sc[t] = __ldg(args.a_scales + gm * nblk + gk / 32);
+          }
+        }
+#pragma unroll
+        for (int t = 0; t < kUnits; ++t) {
+          const int u = tid + t * C::kAThreads;
+          const int m = u >> 3, b = u & 7, r = m & 127;
+          *reinterpret_cast<uint4*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4)) = v[t];
+          sfa[((b >> 2) * C::kRowChunks + (m >> 7)) * kSfChunkBytes + (r & 31) * 16 + (r >> 5) * 4 + (b & 3)] = sc[t];
+        }
+      }
+      fence_proxy_async_smem();  // make the generic stores visible to tcgen05
+      mbar_arrive(full_a(s));
+    }
+
+    // ------------------------------------------------------------------ epilogue: TMEM -> smem fp32
+    bool ok = mbar_wait(accum_bar, 0, timeout);
+    if (!ok) report_error(args.err, kErrWaitAccum);
+    tc_fence_after_sync();
+    const bool have = ok && kt_count > 0 && !*abort_flag;
+    float* staging = reinterpret_cast<float*>(smem);  // [BM][128], reuses the stage buffers
+    const int quarter = warp & 3;                     // TMEM lanes this warp may read
+    constexpr int kColGroups = C::kAWarps / 4;
+    constexpr int kColsPerWarp = BM / kColGroups;
+    const int col0 = ((warp - 2) >> 2) * kColsPerWarp;
+#pragma unroll 1
+    for (int c = col0; c < col0 + kColsPerWarp; c += 16) {
+      uint32_t r[16];
+      if (have) {
+        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c, r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = 0u;
+      }
+#pragma unroll
+      for (int e = 0; e < 16; ++e) staging[(c + e) * kTileN + quarter * 32 + lane] = __uint_as_float(r[e]);
+    }
+  }
+
+  // ---------------------------------------------------------------------- partial tiles visible
+  tc_fence_before_sync();
+  if (splits > 1) cluster_sync_all(); else __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, args.tmem_cols);
+  }
+  if (warp >= 2) {
+    // -------------------------------------------------------------- reduce the splits, store bf16
+    const int tid = threadIdx.x - 64;
+    const int m_valid = min(BM, args.M - m_tile * BM);
+    const int total = m_valid * (kTileN / 4);  // float4 vectors
+    const int n_base = n_tile * kTileN;
+    const bool vec_ok = (args.N % 4) == 0;
+    for (int v = static_cast<int>(rank) * C::kAThreads + tid; v < total; v += splits * C::kAThreads) {
+      const int m = v >> 5, n4 = v & 31;
+      const uint32_t off = m * (kTileN * 4) + n4 * 16;
+      float4 acc;
+      if (splits == 1) {
+        acc = *reinterpret_cast<const float4*>(smem + off);
+      } else {
+        acc = ld_cluster_f4(map_to_rank(sbase + off, 0));
+        for (int src = 1; src < splits; ++src) {
+          const float4 p = ld_cluster_f4(map_to_rank(sbase + off, src));
+          acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
+        }
+      }
+      const int64_t gm = static_cast<int64_t>(m_tile) * BM + m;
+      const int gn = n_base + n4 * 4;
+      __nv_bfloat16* dst = args.c + gm * args.N + gn;
+      if (vec_ok && gn + 3 < args.N) {
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+        uint2 w;
+        w.x = *reinterpret_cast<const uint32_t*>(&lo);
+        w.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(dst) = w;
+      } else {
+        const float e[4] = {acc.x, acc.y, acc.z, acc.w};
+        for (int q = 0; q < 4; ++q)
+          if (gn + q < args.N) dst[q] = __float2bfloat16_rn(e[q]);
+      }
+    }
+  }
+  if (splits > 1) cluster_sync_all();  // peers may still read this CTA's partial tile
+}
+
+// ----------------------------------------------------------------------------- host side
+template <int BM, bool kFused>
+static cudaError_t launch_t(const CUtensorMap& tmap_b, const GemmArgs& args, const mxfp4_plan_t& plan,
+                            cudaStream_t s) {
+  auto kernel = mxfp4_gemm_kernel<BM, kFused>;
+  static int configured_device = -1;  // max dynamic smem set once per device
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (configured_device != dev) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
+    if (e != cudaSuccess) return e;
+    configured_device = dev;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(plan.grid_x, plan.grid_y, plan.grid_z);
+  cfg.blockDim = dim3(plan.threads, 1, 1);
+  cfg.dynamicSmemBytes = plan.smem_bytes;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = plan.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, tmap_b, args);
+}
+
+cudaError_t launch_gemm(const CUtensorMap& tmap_b, const GemmArgs& args, const mxfp4_plan_t& plan,
+                        bool fused, cudaStream_t s) {
+  switch (plan.block_m) {
+    case 32: return fused ? launch_t<32, true>(tmap_b, args, plan, s) : launch_t<32, false>(tmap_b, args, plan, s);
+    case 64: return fused ? launch_t<64, true>(tmap_b, args, plan, s) : launch_t<64, false>(tmap_b, args, plan, s);
+    case 128: return fused ? launch_t<128, true>(tmap_b, args, plan, s) : launch_t<128, false>(tmap_b, args, plan, s);
+    case 256: return fused ? launch_t<256, true>(tmap_b, args, plan, s) : launch_t<256, false>(tmap_b, args, plan, s);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+static int threads_for(int bm) { return bm >= 128 ? 64 + 256 : 64 + 128; }
+
+static SmemLayout layout_for(int bm, int stages) {
+  switch (bm) {
+    case 32: return smem_layout<32>(stages);
+    case 64: return smem_layout<64>(stages);
+    case 128: return smem_layout<128>(stages);
+    default: return smem_layout<256>(stages);
+  }
+}
+
+static int sf_cols_for(int bm) { return 8 + 8 * (bm > 128 ? 2 : 1); }
+
+static uint32_t pow2_at_least(uint32_t x) {
+  uint32_t p = 32;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
+                 mxfp4_plan_t* p) {
+  (void)fused;
+  if (p->block_m != 32 && p->block_m != 64 && p->block_m != 128 && p->block_m != 256) return false;
+  const int64_t k_tiles = ceil_div(K, kTileK);
+  if (p->splits < 1 || p->splits > kMaxSplits || p->splits > k_tiles) return false;
+  const int64_t per = ceil_div(k_tiles, p->splits);
+  // every split gets at least one K tile
+  if ((p->splits - 1) * per >= k_tiles) return false;
+  if (p->stages < 1 || p->stages > per) p->stages = static_cast<int32_t>(per < 6 ? per : 6);
+  p->k_tiles_per_split = static_cast<int32_t>(per);
+  p->grid_x = p->splits;
+  p->grid_y = static_cast<int32_t>(ceil_div(N, kTileN));
+  p->grid_z = static_cast<int32_t>(ceil_div(M, p->block_m));
+  if (p->grid_y > 65535 || p->grid_z > 65535) return false;
+  p->threads = threads_for(p->block_m);
+  const uint32_t tcols = pow2_at_least(p->block_m + p->stages * sf_cols_for(p->block_m));
+  if (tcols > 512) return false;
+  p->tmem_cols = static_cast<int32_t>(tcols);
+  const SmemLayout L = layout_for(p->block_m, p->stages);
+  int64_t smem = static_cast<int64_t>(L.total) + 1024;  // + alignment slack
+  // Tensor-memory allocation blocks while the SM's 512 columns are taken, and
+  // a blocked CTA of one cluster could then wait on a CTA of another cluster
+  // that waits on it.  Each CTA therefore takes shared memory in proportion to
+  // its tensor-memory share (tmem_cols / 512 of the SM's shared memory): the
+  // CTAs that fit on an SM together, from any mix of these kernels, can never
+  // ask for more than 512 columns, and no allocation ever waits.
+  const int64_t per_sm = prop.sharedMemPerMultiprocessor;
+  const int64_t reserved = prop.reservedSharedMemPerBlock;
+  const int64_t floor_smem = (per_sm * tcols + 511) / 512 - reserved;
+  if (smem < floor_smem) smem = floor_smem;
+  smem = (smem + 15) / 16 * 16;
+  if (smem > static_cast<int64_t>(prop.sharedMemPerBlockOptin)) return false;
+  p->smem_bytes = static_cast<int32_t>(smem);
+  return true;
+}
+
+void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
+                  mxfp4_plan_t* p) {
+  *p = mxfp4_plan_t{};
+  p->block_m = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  const int64_t k_tiles = ceil_div(K, kTileK);
+  const int64_t tiles = ceil_div(N, kTileN) * ceil_div(M, p->block_m);
+  int64_t splits = prop.multiProcessorCount / (tiles > 0 ? tiles : 1);
+  if (splits < 1) splits = 1;
+  if (splits > kMaxSplits) splits = kMaxSplits;
+  if (splits > k_tiles) splits = k_tiles;
+  const int64_t per = ceil_div(k_tiles, splits);
+  splits = ceil_div(k_tiles, per);  // no empty split
+  p->splits = static_cast<int32_t>(splits);
+  p->stages = 0;  // finish_plan: min(per, 8)
+  if (!finish_plan(M, N, K, fused, prop, p)) {
+    // fall back to fewer stages (shared memory) -- still the same kernel
+    for (int st = 7; st >= 1; --st) {
+      mxfp4_plan_t q = *p;
+      q.stages = st;
+      if (finish_plan(M, N, K, fused, prop, &q)) {
+        *p = q;
+        return;
+      }
+    }
+  }
+}
+
+}  // namespace mxfp4

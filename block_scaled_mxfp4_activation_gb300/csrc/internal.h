@@ -1,0 +1,83 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/mxfp4.h"
+
+namespace mxfp4 {
+
+// Geometry shared by the packed-weight layout and the GEMM kernel.
+constexpr int kTileN = 128;                      // weight rows per CTA (the MMA's M)
+constexpr int kTileK = 256;                      // K elements per pipeline stage
+constexpr int kTileKBytes = kTileK / 2;          // 128 bytes of codes per row and stage
+constexpr int kSfChunkBytes = 512;               // 128 rows x 4 scales
+constexpr int kSfTileBytes = 2 * kSfChunkBytes;  // scales of one 128 x 256 weight tile
+constexpr int kMaxSplits = 8;                    // portable cluster size
+
+inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+struct PackedLayout {
+  int64_t n_pad;     // rows rounded up to kTileN
+  int64_t k_tiles;   // ceil(K / kTileK)
+  size_t data_bytes; // n_pad * K / 2
+  size_t sf_offset;  // data_bytes rounded up to 1024
+  size_t sf_bytes;   // (n_pad / kTileN) * k_tiles * kSfTileBytes
+  size_t total;
+};
+
+inline PackedLayout packed_layout(int64_t N, int64_t K) {
+  PackedLayout L;
+  L.n_pad = ceil_div(N, kTileN) * kTileN;
+  L.k_tiles = ceil_div(K, kTileK);
+  L.data_bytes = static_cast<size_t>(L.n_pad) * static_cast<size_t>(K / 2);
+  L.sf_offset = (L.data_bytes + 1023) / 1024 * 1024;
+  L.sf_bytes = static_cast<size_t>(L.n_pad / kTileN) * static_cast<size_t>(L.k_tiles) * kSfTileBytes;
+  L.total = L.sf_offset + L.sf_bytes;
+  return L;
+}
+
+struct GemmArgs {
+  const void* a;            // fused: bf16 A [M, lda]; else codes Aq [M, K/2]
+  const uint8_t* a_scales;  // unfused: As [M, K/32]
+  const uint8_t* b_sf;      // packed weight scales
+  __nv_bfloat16* c;         // [M, N]
+  int32_t M, N, K;
+  int64_t lda;              // fused: elements per row of A
+  int32_t k_tiles;          // ceil(K / kTileK)
+  int32_t kt_per_split;
+  int32_t splits;
+  int32_t stages;
+  uint32_t tmem_cols;
+  uint64_t timeout_ns;
+  uint32_t* err;            // device error word
+};
+
+// Launchers (return a CUDA error code; arguments are validated by the caller).
+cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
+                            cudaStream_t s);
+cudaError_t launch_pack_weights(const void* Bq, const void* Bs, int64_t N, int64_t K, void* Bp,
+                                cudaStream_t s);
+cudaError_t launch_unpack_weights(const void* Bp, int64_t N, int64_t K, void* Bq, void* Bs,
+                                  cudaStream_t s);
+cudaError_t launch_diag_wait(uint64_t timeout_ns, cudaStream_t s);
+
+// Fills the derived fields of a plan (block_m, splits, stages given).
+// Returns false if the plan cannot run.
+bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
+                 mxfp4_plan_t* plan);
+void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
+                  mxfp4_plan_t* plan);
+cudaError_t launch_gemm(const CUtensorMap& tmap_b, const GemmArgs& args, const mxfp4_plan_t& plan,
+                        bool fused, cudaStream_t s);
+
+cudaError_t read_device_error(cudaStream_t s, uint32_t* code, bool reset);
+// Address of the device error word on the current device (nullptr on failure).
+uint32_t* device_error_word();
+
+}  // namespace mxfp4

@@ -1,0 +1,176 @@
+// Standalone kernels: activation quantization, the one-time weight relayout
+// and its inverse, the bounded-wait diagnostic, and the device error word.
+#include "internal.h"
+#include "ptx.cuh"
+#include "quant.cuh"
+
+namespace mxfp4 {
+
+// The device error word; kernels receive its address as an argument.
+static __device__ uint32_t g_device_error = 0;
+
+uint32_t* device_error_word() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  static uint32_t* cache[64] = {};
+  if (cache[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_device_error) != cudaSuccess) return nullptr;
+    cache[dev] = static_cast<uint32_t*>(p);
+  }
+  return cache[dev];
+}
+
+// ----------------------------------------------------------------------------- quantize
+// One thread per 8 consecutive elements of a row; 4 lanes per 32-element block;
+// a warp covers 256 consecutive elements (512 contiguous bytes of A).  Rows are
+// K/8 units long and K % 32 == 0, so a block never straddles two rows and the
+// lanes of a block are always all in or all out of range.
+__global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ A, int64_t M,
+                                                       int64_t K, int64_t lda,
+                                                       uint8_t* __restrict__ Aq,
+                                                       uint8_t* __restrict__ As) {
+  const int64_t units_per_row = K / 8;
+  const int64_t unit = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  const bool valid = unit < M * units_per_row;
+  const int64_t row = valid ? unit / units_per_row : 0;
+  const int64_t j = valid ? unit - row * units_per_row : 0;
+  uint4 v = make_uint4(0, 0, 0, 0);
+  if (valid) v = __ldg(reinterpret_cast<const uint4*>(A + row * lda + j * 8));
+  uint32_t byte;
+  const uint32_t codes = quantize_quad(v, &byte);  // every lane takes part in the shuffles
+  if (valid) {
+    *reinterpret_cast<uint32_t*>(Aq + row * (K / 2) + j * 4) = codes;
+    if ((j & 3) == 0) As[row * (K / 32) + j / 4] = static_cast<uint8_t>(byte);
+  }
+}
+
+cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
+                            cudaStream_t s) {
+  const int64_t units = M * (K / 8);
+  const int threads = 256;
+  const int64_t blocks = ceil_div(units, threads);
+  quantize_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
+      static_cast<const uint16_t*>(A), M, K, lda, static_cast<uint8_t*>(Aq), static_cast<uint8_t*>(As));
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- weight relayout
+// Position of scale (n, j) -- row n, 32-element block j -- in the packed scale
+// region: tile (n / 128, j / 8), chunk (j % 8) / 4, byte (r % 32) * 16 +
+// (r / 32) * 4 + j % 4 with r = n % 128.  This is the 128-row x 4-scale chunk
+// that one tcgen05.cp 32x128b.warpx4 moves into tensor memory.
+__device__ __forceinline__ size_t packed_sf_index(int64_t n, int64_t j, int64_t k_tiles) {
+  const int64_t tile = (n / kTileN) * k_tiles + j / 8;
+  const int64_t r = n % kTileN;
+  return static_cast<size_t>(tile) * kSfTileBytes + ((j % 8) / 4) * kSfChunkBytes + (r % 32) * 16 +
+         (r / 32) * 4 + (j % 4);
+}
+
+__global__ void pack_codes_kernel(const uint4* __restrict__ bq, int64_t N, int64_t n_pad,
+                                  int64_t row_vecs, uint4* __restrict__ out) {
+  const int64_t total = n_pad * row_vecs;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = i / row_vecs;
+    out[i] = (n < N) ? bq[i] : make_uint4(0, 0, 0, 0);
+  }
+}
+
+__global__ void pack_scales_kernel(const uint8_t* __restrict__ bs, int64_t N, int64_t n_pad,
+                                   int64_t nblk, int64_t k_tiles, uint8_t* __restrict__ sf) {
+  const int64_t per_row = k_tiles * 8;
+  const int64_t total = n_pad * per_row;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t n = i / per_row, j = i % per_row;
+    sf[packed_sf_index(n, j, k_tiles)] = (n < N && j < nblk) ? bs[n * nblk + j] : 0;
+  }
+}
+
+__global__ void unpack_kernel(const uint8_t* __restrict__ bp, int64_t N, int64_t K, size_t sf_offset,
+                              int64_t k_tiles, uint8_t* __restrict__ bq, uint8_t* __restrict__ bs) {
+  const int64_t kh = K / 2, nblk = K / 32;
+  const int64_t total = N * kh;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    bq[i] = bp[i];
+    const int64_t n = i / kh, b = i % kh;
+    if (b % 16 == 0) bs[n * nblk + b / 16] = bp[sf_offset + packed_sf_index(n, b / 16, k_tiles)];
+  }
+}
+
+static unsigned grid_for(int64_t work, int threads) {
+  int64_t b = ceil_div(work, threads);
+  if (b > 65536) b = 65536;
+  if (b < 1) b = 1;
+  return static_cast<unsigned>(b);
+}
+
+cudaError_t launch_pack_weights(const void* Bq, const void* Bs, int64_t N, int64_t K, void* Bp,
+                                cudaStream_t s) {
+  const PackedLayout L = packed_layout(N, K);
+  uint8_t* out = static_cast<uint8_t*>(Bp);
+  const int64_t row_vecs = K / 32;  // 16-byte vectors per row of codes
+  pack_codes_kernel<<<grid_for(L.n_pad * row_vecs, 256), 256, 0, s>>>(
+      static_cast<const uint4*>(Bq), N, L.n_pad, row_vecs, reinterpret_cast<uint4*>(out));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (L.sf_offset > L.data_bytes) {
+    e = cudaMemsetAsync(out + L.data_bytes, 0, L.sf_offset - L.data_bytes, s);
+    if (e != cudaSuccess) return e;
+  }
+  pack_scales_kernel<<<grid_for(L.n_pad * L.k_tiles * 8, 256), 256, 0, s>>>(
+      static_cast<const uint8_t*>(Bs), N, L.n_pad, K / 32, L.k_tiles, out + L.sf_offset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_unpack_weights(const void* Bp, int64_t N, int64_t K, void* Bq, void* Bs,
+                                  cudaStream_t s) {
+  const PackedLayout L = packed_layout(N, K);
+  unpack_kernel<<<grid_for(N * (K / 2), 256), 256, 0, s>>>(
+      static_cast<const uint8_t*>(Bp), N, K, L.sf_offset, L.k_tiles, static_cast<uint8_t*>(Bq),
+      static_cast<uint8_t*>(Bs));
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------------------- diagnostics
+// Waits on an mbarrier that expects two arrivals and gets one, so its phase
+// never completes; the bounded wait gives up after timeout_ns and reports.
+__global__ void diag_wait_kernel(uint64_t timeout_ns, uint32_t* err) {
+  __shared__ __align__(8) uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 2);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    mbar_arrive(b);
+    if (!mbar_wait(b, 0, timeout_ns)) report_error(err, kErrDiag);
+  }
+}
+
+cudaError_t launch_diag_wait(uint64_t timeout_ns, cudaStream_t s) {
+  uint32_t* err = device_error_word();
+  if (err == nullptr) return cudaErrorInvalidSymbol;
+  diag_wait_kernel<<<1, 32, 0, s>>>(timeout_ns, err);
+  return cudaGetLastError();
+}
+
+cudaError_t read_device_error(cudaStream_t s, uint32_t* code, bool reset) {
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return e;
+  uint32_t v = 0;
+  e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+  if (e != cudaSuccess) return e;
+  if (reset && v != 0) {
+    const uint32_t zero = 0;
+    e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    if (e != cudaSuccess) return e;
+  }
+  *code = v;
+  return cudaSuccess;
+}
+
+}  // namespace mxfp4

@@ -1,0 +1,165 @@
+/*
+ * libmxfp4 -- MXFP4 linear layer on one NVIDIA GB300 (sm_103a).
+ *
+ * Computes C[M, N] = A[M, K] * B[N, K]^T with bf16 output, where A is a bf16
+ * activation quantized on the fly to MXFP4 and B is a weight matrix quantized
+ * to MXFP4 ahead of time.  MXFP4 (OCP Microscaling v1.0): each run of 32
+ * consecutive K elements of a row shares one E8M0 scale byte (value
+ * 2^(byte - 127)); each element is an E2M1 code (sign | 2-bit exponent |
+ * 1-bit mantissa; magnitudes 0, .5, 1, 1.5, 2, 3, 4, 6), two codes per byte,
+ * the even K index in the low nibble.  This is the problem of the
+ * amd-mxfp4-mm leaderboard (kernelindex.com submissions 748756, 721672,
+ * 754569, 755056, 733989): `custom_kernel((A, B, B_q, B_shuffle,
+ * B_scale_sh)) -> C`.
+ *
+ * Conventions for every call:
+ *   - Pointers marked "device" are CUDA device pointers on the current device;
+ *     the caller allocates and owns every buffer.  No call allocates device
+ *     memory, so every compute call may be captured in a CUDA graph.
+ *   - Compute calls are asynchronous on `stream` (NULL = legacy default stream)
+ *     and return after the launch; their results are ready when the stream is.
+ *   - Arguments are checked on the host before anything is launched; a call
+ *     that returns an error status has launched nothing.  There is no fallback
+ *     path: a shape or alignment outside the contract is an error.
+ *   - Sizes are int64_t element counts.  K must be a positive multiple of 32.
+ *     Every device pointer must be 16-byte aligned.
+ *   - Device-side waits are bounded (about one second by default).  A wait
+ *     that runs out sets the library's device error word and the kernel
+ *     finishes without its result; read the word with mxfp4_device_error().
+ */
+#ifndef MXFP4_H_
+#define MXFP4_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t / CUstream). */
+typedef struct CUstream_st* mxfp4_stream_t;
+
+typedef enum {
+  MXFP4_OK = 0,
+  MXFP4_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, K % 32 != 0, bad plan */
+  MXFP4_ERR_UNSUPPORTED_SHAPE = 2,  /* a size beyond the library's limits */
+  MXFP4_ERR_MISALIGNED = 3,         /* a pointer or leading dimension not 16-byte aligned */
+  MXFP4_ERR_WORKSPACE_TOO_SMALL = 4,
+  MXFP4_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+  MXFP4_ERR_DEVICE_TIMEOUT = 6,     /* a device-side bounded wait ran out */
+  MXFP4_ERR_UNSUPPORTED_DEVICE = 7  /* the current device is not sm_103 */
+} mxfp4_status_t;
+
+/* Tile plan of one GEMM launch (see mxfp4_gemm_plan). */
+typedef struct {
+  int32_t block_m;    /* activation rows per CTA = the MMA's N: 32, 64, 128 or 256 */
+  int32_t splits;     /* K splits per output tile = CTAs per thread-block cluster, 1..8 */
+  int32_t stages;     /* shared-memory pipeline depth in K tiles of 256 */
+  int32_t k_tiles_per_split;
+  int32_t grid_x, grid_y, grid_z; /* splits, N tiles of 128, M tiles of block_m */
+  int32_t threads;    /* threads per CTA */
+  int32_t smem_bytes; /* dynamic shared memory per CTA */
+  int32_t tmem_cols;  /* tensor-memory columns allocated per CTA */
+} mxfp4_plan_t;
+
+/* ---------------------------------------------------------------------------
+ * mxfp4_quantize -- A (bf16) -> MXFP4 codes + E8M0 scales.
+ *
+ * The rule of `hw_pack_mxfp4` (submission 748756) and "Software MXFP4 quant"
+ * (submission 755056): per row and 32-element block, amax = max |x|;
+ * u = (bits(amax) + 0x200000) & 0xFF800000; s = clamp(exponent(u) - 129,
+ * -127, 127); scale byte = s + 127; each element x -> E2M1(x * 2^-s) with
+ * round-to-nearest-even, saturating at 6, sign kept (so -0 -> 0x8).
+ *
+ *   A   device, bf16 [M, lda] row-major (first K columns used); lda % 8 == 0
+ *   Aq  device, uint8 [M, K/2] row-major, byte = code[2i] | code[2i+1] << 4
+ *   As  device, uint8 [M, K/32] row-major
+ * M >= 1.  Returns MXFP4_OK or an error status (nothing launched).
+ * ------------------------------------------------------------------------- */
+mxfp4_status_t mxfp4_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
+                              mxfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Packed weights: the one-time relayout of a pre-quantized B (the pages cache
+ * such a relayout per weight, e.g. the linearised-weight cache of submission
+ * 748756) into the layout the GEMM streams with TMA:
+ *   - codes: [roundup(N,128), K/2] bytes, rows >= N zero;
+ *   - scales: for each 128-row N tile and 256-wide K tile, 1024 bytes: two
+ *     512-byte chunks (K sub-blocks of 128), byte (r%32)*16 + (r/32)*4 + j for
+ *     tile row r and scale j = 0..3 of the chunk; padding scales are 0.
+ * The buffer is opaque to callers; its size is mxfp4_packed_weight_bytes().
+ * ------------------------------------------------------------------------- */
+size_t mxfp4_packed_weight_bytes(int64_t N, int64_t K);
+
+/*   Bq      device, uint8 [N, K/2] (natural layout, as mxfp4_quantize writes it)
+ *   Bs      device, uint8 [N, K/32]
+ *   Bpacked device, mxfp4_packed_weight_bytes(N, K) bytes, written entirely. */
+mxfp4_status_t mxfp4_pack_weights(const void* Bq, const void* Bs, int64_t N, int64_t K, void* Bpacked,
+                                  mxfp4_stream_t stream);
+
+/* Inverse of mxfp4_pack_weights (for checking a packed buffer). */
+mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, void* Bq, void* Bs,
+                                    mxfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * GEMM.  C[m, n] = sum_k deq(A)[m, k] * deq(B)[n, k], block-scaled FP4 x FP4
+ * products accumulated in fp32 (the pages' `tl.dot_scaled(a, a_scale, "e2m1",
+ * b, b_scale, "e2m1", acc)`), K splits summed in fp32 in a fixed order
+ * (deterministic), rounded to bf16 (nearest even).
+ *
+ *   Aq, As   device, the outputs of mxfp4_quantize for A [M, K]
+ *   A        device, bf16 [M, lda]; lda % 8 == 0 (fused entry only)
+ *   Bpacked  device, the output of mxfp4_pack_weights for the same N, K
+ *   C        device, bf16 [M, N] row-major, fully overwritten
+ *   ws, ws_bytes  scratch; the current plans need none (NULL, 0 is valid);
+ *            mxfp4_workspace_bytes() gives the requirement.
+ * M, N >= 1.  Returns MXFP4_OK or an error status (nothing launched).
+ * ------------------------------------------------------------------------- */
+size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+mxfp4_status_t mxfp4_gemm(const void* Aq, const void* As, const void* Bpacked, void* C, int64_t M,
+                          int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
+
+/* The fused entry: quantizes A inside the GEMM kernel (no global Aq/As), with
+ * the same rule and bit-identical codes as mxfp4_quantize. */
+mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M,
+                                int64_t N, int64_t K, void* ws, size_t ws_bytes,
+                                mxfp4_stream_t stream);
+
+/* The plan the two GEMM entries would use for (M, N, K); fused != 0 for the
+ * fused entry.  Host only, launches nothing. */
+mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan);
+
+/* The GEMM entries with an explicit plan: only block_m, splits and stages are
+ * read (the rest is derived); a plan the device cannot run is rejected with
+ * MXFP4_ERR_INVALID_ARG.  fused != 0 reads A/lda, else Aq/As. */
+mxfp4_status_t mxfp4_gemm_with_plan(const void* A_or_Aq, int64_t lda, const void* As,
+                                    const void* Bpacked, void* C, int64_t M, int64_t N, int64_t K,
+                                    int fused, const mxfp4_plan_t* plan, mxfp4_stream_t stream);
+
+/* ---------------------------------------------------------------------------
+ * Errors and diagnostics.
+ * ------------------------------------------------------------------------- */
+const char* mxfp4_status_string(mxfp4_status_t status);
+
+/* Synchronises `stream`, then reads the device error word (0 = no device-side
+ * failure since the last reset) into *code and, if reset != 0, clears it.
+ * Returns MXFP4_ERR_DEVICE_TIMEOUT if the word is non-zero, else MXFP4_OK. */
+mxfp4_status_t mxfp4_device_error(mxfp4_stream_t stream, int reset, uint32_t* code);
+
+/* Limit, in nanoseconds, of every device-side wait in kernels launched after
+ * this call (default 1e9; 0 restores the default). */
+mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns);
+
+/* Diagnostic: launches one tiny kernel whose wait can never complete (an
+ * mbarrier nothing arrives on) and that therefore gives up after the current
+ * wait limit and sets the device error word.  Lets a caller check that bounded
+ * waits end and report instead of hanging. */
+mxfp4_status_t mxfp4_diag_wait_timeout(mxfp4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXFP4_H_ */

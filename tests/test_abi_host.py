@@ -1,0 +1,93 @@
+"""Host-only checks of the C ABI: the library builds and loads, exports every
+function include/mxfp4.h declares, and rejects bad arguments with the
+documented status before touching a GPU."""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import block_scaled_mxfp4_activation_gb300 as mx
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "mxfp4.h")
+
+OK, INVALID, UNSUPPORTED, MISALIGNED, WS_SMALL, CUDA, TIMEOUT, DEVICE = range(8)
+
+
+def declared_functions() -> list[str]:
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(mxfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    return mx.load_library()
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("mxfp4_quantize", "mxfp4_pack_weights", "mxfp4_gemm", "mxfp4_quant_gemm",
+                     "mxfp4_packed_weight_bytes", "mxfp4_workspace_bytes", "mxfp4_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+        assert ctypes.cast(getattr(lib, name), ctypes.c_void_p).value
+
+
+def test_status_strings(lib):
+    for s in range(8):
+        assert lib.mxfp4_status_string(s)
+    assert lib.mxfp4_status_string(99) == b"unknown status"
+
+
+def test_packed_weight_bytes_layout(lib):
+    # codes [roundup(N,128), K/2] then scales at a 1 KB boundary:
+    # one 1 KB block per 128-row x 256-column tile
+    for N, K in ((2880, 512), (2112, 7168), (7168, 2048), (3072, 1536), (1, 32), (129, 288)):
+        n_pad = -(-N // 128) * 128
+        data = n_pad * K // 2
+        sf_off = -(-data // 1024) * 1024
+        expect = sf_off + (n_pad // 128) * (-(-K // 256)) * 1024
+        assert lib.mxfp4_packed_weight_bytes(N, K) == expect
+    assert lib.mxfp4_packed_weight_bytes(16, 48) == 0  # K % 32 != 0
+    assert lib.mxfp4_packed_weight_bytes(0, 64) == 0
+    assert lib.mxfp4_workspace_bytes(16, 2112, 7168) == 0
+
+
+def test_argument_checks_launch_nothing(lib):
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: checks fail first
+    odd = ctypes.c_void_p(0x10001)
+    assert lib.mxfp4_quantize(None, 4, 64, 64, fake, fake, None) == INVALID
+    assert lib.mxfp4_quantize(fake, 4, 48, 48, fake, fake, None) == INVALID  # K % 32
+    assert lib.mxfp4_quantize(fake, 4, 64, 32, fake, fake, None) == INVALID  # lda < K
+    assert lib.mxfp4_quantize(fake, 0, 64, 64, fake, fake, None) == INVALID
+    assert lib.mxfp4_quantize(odd, 4, 64, 64, fake, fake, None) == MISALIGNED
+    assert lib.mxfp4_quantize(fake, 4, 64, 68, fake, fake, None) == MISALIGNED  # lda % 8
+    assert lib.mxfp4_pack_weights(fake, None, 128, 64, fake, None) == INVALID
+    assert lib.mxfp4_pack_weights(fake, fake, 128, 80, fake, None) == INVALID
+    assert lib.mxfp4_pack_weights(odd, fake, 128, 64, fake, None) == MISALIGNED
+    assert lib.mxfp4_gemm(fake, None, fake, fake, 4, 128, 64, None, 0, None) == INVALID
+    assert lib.mxfp4_gemm(fake, fake, fake, fake, 4, 128, 40, None, 0, None) == INVALID
+    assert lib.mxfp4_gemm(fake, fake, odd, fake, 4, 128, 64, None, 0, None) == MISALIGNED
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, None, 4, 128, 64, None, 0, None) == INVALID
+    assert lib.mxfp4_quant_gemm(fake, 60, fake, fake, 4, 128, 64, None, 0, None) == INVALID  # lda < K
+    assert lib.mxfp4_quant_gemm(fake, 68, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED  # lda % 8
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 4, 0, 64, None, 0, None) == INVALID
+    assert lib.mxfp4_quant_gemm(fake, 1 << 40, fake, fake, 1 << 31, 128, 1 << 31, None, 0, None) == UNSUPPORTED
+    assert lib.mxfp4_gemm_plan(4, 128, 64, 1, None) == INVALID
+    assert lib.mxfp4_device_error(None, 0, None) == INVALID
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+
+    with pytest.raises(TypeError):
+        mx.quantize(torch.zeros(4, 64, dtype=torch.bfloat16))
+    with pytest.raises(TypeError):
+        mx.quant_gemm(torch.zeros(4, 64, dtype=torch.bfloat16), mx.PackedWeight(torch.zeros(8, dtype=torch.uint8), 128, 64))

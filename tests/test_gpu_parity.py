@@ -1,0 +1,212 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bars: quantized codes and scales bit-exact; C within
+|C - C_ref| <= 8e-3 |C_ref| + 1e-2 rms(C_ref), C_ref the oracle's fp64 sums.
+Shapes: tiny and ragged ones the oracle finishes in seconds (several tiles,
+tails in M, N and K), and the six leaderboard shapes at full size checked
+element by element on samples."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import block_scaled_mxfp4_activation_gb300 as mx
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+RTOL, ATOL_RMS = 8e-3, 1e-2
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    mx.load_library()
+    torch.cuda.set_device(0)
+    assert mx.device_error(reset=True) == 0
+    yield
+    assert mx.device_error(reset=True) == 0, "a device-side wait timed out during the tests"
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_np_to_f64(u: np.ndarray) -> np.ndarray:
+    return (u.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def check_close(got_bf16: torch.Tensor, ref64: np.ndarray, what: str):
+    got = got_bf16.float().cpu().numpy().astype(np.float64)
+    rms = float(np.sqrt(np.mean(ref64 ** 2))) if ref64.size else 0.0
+    err = np.abs(got - ref64)
+    bound = RTOL * np.abs(ref64) + ATOL_RMS * rms
+    bad = err > bound
+    assert not bad.any(), (f"{what}: {int(bad.sum())} of {bad.size} outside tolerance; worst err "
+                           f"{float(err.max()):.4g}, rms {rms:.4g}")
+
+
+def quantized_weight(oracle_mod, B: torch.Tensor):
+    """B quantized by the oracle (the harness's pre-quantized weight), packed on the GPU."""
+    bq, bs = oracle_mod.quantize(B)
+    W = mx.pack_weights(torch.from_numpy(bq).cuda(), torch.from_numpy(bs).cuda())
+    return bq, bs, mx.PackedWeight(W, B.shape[0], B.shape[1])
+
+
+# ----------------------------------------------------------------------------- quantize
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_quantize_bitexact_workloads(oracle_mod, name):
+    A, B = workloads.make_inputs(name)
+    for X in (A, B):
+        q, s = mx.quantize(X.cuda())
+        rq, rs = oracle_mod.quantize(X)
+        assert np.array_equal(s.cpu().numpy(), rs)
+        assert np.array_equal(q.cpu().numpy(), rq)
+
+
+def test_quantize_bitexact_every_bf16_value(oracle_mod):
+    pats = u16(workloads.all_bf16_patterns())
+    rng = np.random.default_rng(0)
+    for anchor in (None, 0x7F7F, 0x3F80, 0x0080, 0x0001):
+        x = pats.copy() if anchor is None else pats.copy()
+        if anchor is None:
+            x = x[rng.permutation(x.size)]
+        blocks = x.reshape(-1, 32).copy()
+        if anchor is not None:
+            blocks[:, 0] = anchor
+        A = torch.from_numpy(blocks.reshape(-1, 256).view(np.int16)).view(torch.bfloat16)
+        q, s = mx.quantize(A.cuda())
+        rq, rs = oracle_mod.quantize(A)
+        assert np.array_equal(s.cpu().numpy(), rs), anchor
+        assert np.array_equal(q.cpu().numpy(), rq), anchor
+
+
+@pytest.mark.parametrize("M,K,lda", [(1, 32, 32), (2, 64, 72), (3, 96, 96), (5, 288, 296), (4, 7168, 7168),
+                                     (33, 160, 160), (1, 4096, 4104)])
+def test_quantize_ragged_and_strided(oracle_mod, M, K, lda):
+    full = workloads.make_activation(M, lda, seed=M * 1000 + K)
+    full[:, :K] *= torch.linspace(1e-3, 1e3, K).to(torch.bfloat16)  # varied block scales
+    Ad = full.cuda()[:, :K]
+    assert Ad.stride(0) == lda
+    q, s = mx.quantize(Ad)
+    rq, rs = oracle_mod.quantize(full[:, :K].contiguous())
+    assert np.array_equal(s.cpu().numpy(), rs) and np.array_equal(q.cpu().numpy(), rq)
+
+
+# ----------------------------------------------------------------------------- weight packing
+@pytest.mark.parametrize("N,K", [(1, 32), (129, 288), (2112, 7168), (300, 544)])
+def test_pack_unpack_round_trip(N, K):
+    g = torch.Generator().manual_seed(N + K)
+    Bq = torch.randint(0, 256, (N, K // 2), dtype=torch.uint8, generator=g)
+    Bs = torch.randint(0, 255, (N, K // 32), dtype=torch.uint8, generator=g)
+    P = mx.pack_weights(Bq.cuda(), Bs.cuda())
+    assert P.numel() == mx.packed_weight_bytes(N, K)
+    q, s = mx.unpack_weights(P, N, K)
+    assert torch.equal(q.cpu(), Bq) and torch.equal(s.cpu(), Bs)
+    # padding rows of the code region are zero
+    n_pad = -(-N // 128) * 128
+    assert int(P[N * K // 2:n_pad * K // 2].count_nonzero()) == 0
+
+
+# ----------------------------------------------------------------------------- GEMM, small shapes
+SMALL = [
+    (1, 128, 64), (4, 256, 512), (5, 300, 288), (16, 200, 7168 // 4), (32, 128, 256), (37, 257, 544),
+    (64, 384, 1024), (100, 130, 96), (128, 128, 512), (130, 260, 320), (256, 256, 256), (300, 129, 64),
+]
+
+
+@pytest.mark.parametrize("M,N,K", SMALL)
+def test_gemm_small_full_parity(oracle_mod, M, N, K):
+    A, B = workloads.make_random(M, N, K, seed=M * 7 + N * 3 + K)
+    bq, bs, W = quantized_weight(oracle_mod, B)
+    aq, as_, c64, c16 = oracle_mod.quant_gemm(A, bq, bs)
+    Ad = A.cuda()
+    C_fused = mx.quant_gemm(Ad, W)
+    Aq, As = mx.quantize(Ad)
+    assert np.array_equal(Aq.cpu().numpy(), aq) and np.array_equal(As.cpu().numpy(), as_)
+    C_unfused = mx.gemm(Aq, As, W)
+    torch.cuda.synchronize()
+    check_close(C_fused, c64, f"fused {M}x{N}x{K}")
+    check_close(C_unfused, c64, f"unfused {M}x{N}x{K}")
+    # the fused kernel quantizes exactly like the standalone quantizer: same sums
+    assert torch.equal(C_fused, C_unfused)
+
+
+def test_gemm_every_plan_agrees(oracle_mod):
+    M, N, K = 40, 384, 2048
+    A, B = workloads.make_random(M, N, K, seed=99)
+    bq, bs, W = quantized_weight(oracle_mod, B)
+    _, _, c64, _ = oracle_mod.quant_gemm(A, bq, bs)
+    Ad = A.cuda()
+    Aq, As = mx.quantize(Ad)
+    results = []
+    for bm in (32, 64, 128, 256):
+        for splits in (1, 2, 4, 8):
+            for stages in (1, 2, 3):
+                plan = {"block_m": bm, "splits": splits, "stages": stages}
+                for fused in (True, False):
+                    C = mx.gemm_with_plan(Ad if fused else Aq, None if fused else As, W, plan, fused)
+                    check_close(C, c64, f"plan {plan} fused={fused}")
+                    results.append(C)
+    assert len(results) == 96
+
+
+def test_gemm_deterministic_and_graph_replay(oracle_mod):
+    M, N, K = 16, 2112, 7168
+    A, B = workloads.make_random(M, N, K, seed=5, b_std=0.02, outlier_frac=0.01)
+    _, _, W = quantized_weight(oracle_mod, B)
+    Ad = A.cuda()
+    C1 = mx.quant_gemm(Ad, W)
+    C2 = mx.quant_gemm(Ad, W)
+    assert torch.equal(C1, C2)
+    out = torch.empty_like(C1)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        mx.quant_gemm(Ad, W, out=out)  # warm (lazy module load) outside the capture
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        mx.quant_gemm(Ad, W, out=out)
+    out.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(out, C1)
+
+
+# ----------------------------------------------------------------------------- GEMM, full sizes
+@pytest.mark.parametrize("name", list(workloads.WORKLOADS))
+def test_gemm_full_size_sampled(oracle_mod, name):
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.make_inputs(w)
+    bq, bs, W = quantized_weight(oracle_mod, B)
+    aq, as_ = oracle_mod.quantize(A)
+    Ad = A.cuda()
+    C = mx.quant_gemm(Ad, W).cpu()
+    Aq, As = mx.quantize(Ad)
+    C_unfused = mx.gemm(Aq, As, W).cpu()
+    assert torch.equal(C, C_unfused)
+    rng = np.random.default_rng(w.seed)
+    ms = np.concatenate([rng.integers(0, w.M, 3000), np.full(64, w.M - 1), np.zeros(64, np.int64)])
+    ns = np.concatenate([rng.integers(0, w.N, 3000), w.N - 1 - np.arange(64), np.arange(64)])
+    c64, _ = oracle_mod.gemm_sampled(aq, as_, bq, bs, ms, ns)
+    check_close(C[ms, ns], c64, f"{name} sampled")
+
+
+# ----------------------------------------------------------------------------- bounded waits
+def test_bounded_wait_reports_instead_of_hanging():
+    assert mx.device_error(reset=True) == 0
+    mx.set_wait_timeout_ns(20_000_000)  # 20 ms
+    try:
+        mx.diag_wait_timeout()
+        code = mx.device_error(reset=True)
+    finally:
+        mx.set_wait_timeout_ns(0)
+    assert code == 1 << 5
+    assert mx.device_error(reset=True) == 0
+    # the context is still usable
+    x = torch.ones(4, 64, dtype=torch.bfloat16, device="cuda")
+    q, s = mx.quantize(x)
+    assert int(s[0, 0]) == 125
