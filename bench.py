@@ -263,8 +263,8 @@ def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
     per_elem = spent / done
     us = (t_quant + per_elem * w.M * w.N) * 1e6
     return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{name}: full A quantization + {done} of {w.M * w.N} outputs (fp64, ascending k), "
-                      f"{spent:.1f} s, scaled to M*N"}
+            "sample": f"{name}: one full A quantization + {done} randomly sampled output elements "
+                      f"(of {w.M * w.N} per call; fp64, ascending k) in {spent:.1f} s, scaled to M*N"}
 
 
 def run_ours(args) -> dict:
