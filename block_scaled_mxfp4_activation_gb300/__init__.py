@@ -24,7 +24,7 @@ __all__ = [
     "MXFP4Error", "PackedWeight", "load_library", "library_path", "quantize", "packed_weight_bytes",
     "pack_weights", "unpack_weights", "quantize_weights", "gemm", "quant_gemm", "gemm_plan",
     "gemm_with_plan", "workspace_bytes", "device_error", "set_wait_timeout_ns", "diag_wait_timeout",
-    "status_string", "Plan",
+    "status_string", "Plan", "set_programmatic_launch",
 ]
 
 MXFP4_OK = 0
@@ -85,6 +85,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             "mxfp4_device_error": ([S, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], st),
             "mxfp4_set_wait_timeout_ns": ([ctypes.c_uint64], st),
             "mxfp4_diag_wait_timeout": ([S], st),
+            "mxfp4_set_programmatic_launch": ([ctypes.c_int], st),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -258,6 +259,11 @@ def device_error(reset: bool = True, stream=None) -> int:
 
 def set_wait_timeout_ns(ns: int) -> None:
     _call("mxfp4_set_wait_timeout_ns", int(ns))
+
+
+def set_programmatic_launch(enable: bool) -> None:
+    """Programmatic dependent launch of the GEMM entries (default on)."""
+    _call("mxfp4_set_programmatic_launch", int(bool(enable)))
 
 
 def diag_wait_timeout(stream=None) -> None:

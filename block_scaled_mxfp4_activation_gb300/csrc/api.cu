@@ -11,6 +11,7 @@ namespace mxfp4 {
 namespace {
 
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
+std::atomic<int> g_programmatic{1};
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -71,6 +72,35 @@ bool encode_weight_map(const void* bpacked, int64_t N, int64_t K, CUtensorMap* m
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the activation for one GEMM launch: bf16 [M, lda] with
+// 256 x block_m boxes, no swizzle (the fused entry quantizes from shared
+// memory), or codes [M, K/2] with 128-byte x block_m boxes and the 128-byte
+// swizzle (landing directly in the MMA operand layout).  Rows past M and
+// columns past K read as zero.
+bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, bool fused, int block_m,
+                           CUtensorMap* map) {
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return false;
+  cuuint32_t elem_strides[2] = {1, 1};
+  CUresult r;
+  if (fused) {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * 2)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(block_m)};
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  } else {
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M)};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKBytes), static_cast<cuuint32_t>(block_m)};
+    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a), dims, strides, box, elem_strides,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  }
+  return r == CUDA_SUCCESS;
+}
+
 constexpr int64_t kMaxDim = int64_t(1) << 30;
 
 mxfp4_status_t check_mnk(int64_t M, int64_t N, int64_t K) {
@@ -106,8 +136,9 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
     default_plan(M, N, K, fused, dev->prop, &plan);
     if (plan.threads == 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   }
-  CUtensorMap map;
+  CUtensorMap map, amap;
   if (!encode_weight_map(bpacked, N, K, &map)) return MXFP4_ERR_CUDA;
+  if (!encode_activation_map(a, M, K, fused ? lda : K / 2, fused, plan.block_m, &amap)) return MXFP4_ERR_CUDA;
   GemmArgs g{};
   g.a = a;
   g.a_scales = static_cast<const uint8_t*>(as);
@@ -126,7 +157,9 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   g.timeout_ns = g_timeout_ns.load();
   g.err = device_error_word();
   if (g.err == nullptr) return MXFP4_ERR_CUDA;
-  return launch_gemm(map, g, plan, fused, stream) == cudaSuccess ? MXFP4_OK : MXFP4_ERR_CUDA;
+  return launch_gemm(map, amap, g, plan, fused, g_programmatic.load() != 0, stream) == cudaSuccess
+             ? MXFP4_OK
+             : MXFP4_ERR_CUDA;
 }
 
 }  // namespace
@@ -244,6 +277,11 @@ mxfp4_status_t mxfp4_device_error(mxfp4_stream_t stream, int reset, uint32_t* co
 
 mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns == 0 ? 1000000000ull : ns);
+  return MXFP4_OK;
+}
+
+mxfp4_status_t mxfp4_set_programmatic_launch(int enable) {
+  g_programmatic.store(enable != 0 ? 1 : 0);
   return MXFP4_OK;
 }
 

@@ -11,11 +11,14 @@
 //   - the output tile is C^T[128 weight rows, block_m activation rows]: the
 //     weights are the MMA's A operand (M = 128) and the activations its B
 //     operand (N = block_m), so a handful of tokens still fills the MMA;
-//   - warp 0 streams 128 x 256 tiles of packed weight codes with TMA (128-byte
-//     swizzle) plus their 1 KB of pre-arranged scales with a bulk copy;
-//   - warps 2.. quantize the bf16 activation tile straight into shared memory,
-//     in the operand's swizzled layout, and write its scales in the
-//     tensor-memory scale-chunk layout;
+//   - warp 0 issues every load of the CTA at once with TMA: per 256-wide K
+//     tile, the 128 x 128-byte box of weight codes (128-byte swizzle), the
+//     tile's 1 KB of pre-arranged weight scales (bulk copy) and the activation
+//     tile -- bf16 for the fused entry, codes straight into the MMA operand's
+//     swizzled layout for the unfused one;
+//   - warps 2.. quantize the staged bf16 activation tile in shared memory (or
+//     place the pre-quantized scales), writing codes in the operand's swizzled
+//     layout and scales in the tensor-memory scale-chunk layout;
 //   - warp 1 moves both scale sets to tensor memory (tcgen05.cp) and issues
 //     four K = 64 block-scaled MMAs per stage into an fp32 accumulator in
 //     tensor memory;
@@ -24,19 +27,23 @@
 //     partials through distributed shared memory in a fixed order
 //     (deterministic, no global workspace, no second kernel);
 //   - bf16 is written with 8-byte coalesced stores.
+//
+// Back-to-back calls overlap through programmatic dependent launch: the next
+// call's CTAs set up and prefetch their operands into L2 while this one ends.
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
 
 namespace mxfp4 {
 
-template <int BM>
+template <int BM, bool kFused>
 struct TileCfg {
   static constexpr int kRowChunks = BM > 128 ? 2 : 1;             // 128-row scale chunks of A
   static constexpr int kBTileBytes = kTileN * kTileKBytes;         // 16 KB of weight codes
   static constexpr int kATileBytes = BM * kTileKBytes;             // activation codes
+  static constexpr int kAbfBytes = kFused ? BM * kTileK * 2 : 0;   // bf16 activation staging
   static constexpr int kSfaStageBytes = 2 * kRowChunks * kSfChunkBytes;
-  static constexpr int kStageBytes = kBTileBytes + kATileBytes + kSfTileBytes + kSfaStageBytes;
+  static constexpr int kStageBytes = kBTileBytes + kATileBytes + kAbfBytes + kSfTileBytes + kSfaStageBytes;
   static constexpr int kAWarps = BM >= 128 ? 8 : 4;                // producer / epilogue warps
   static constexpr int kAThreads = kAWarps * 32;
   static constexpr int kThreads = 64 + kAThreads;
@@ -58,44 +65,52 @@ __device__ __forceinline__ uint32_t mxf4_idesc(uint32_t scale_id) {
 
 // Shared-memory layout of one CTA (offsets from a 1024-byte aligned base).
 struct SmemLayout {
-  uint32_t a_off, sfw_off, sfa_off, bar_off, total;
+  uint32_t a_off, abf_off, sfw_off, sfa_off, bar_off, total;
 };
 
-template <int BM>
+template <int BM, bool kFused>
 __host__ __device__ inline SmemLayout smem_layout(int stages) {
-  using C = TileCfg<BM>;
+  using C = TileCfg<BM, kFused>;
   SmemLayout L;
   L.a_off = stages * C::kBTileBytes;
-  L.sfw_off = L.a_off + stages * C::kATileBytes;
+  L.abf_off = L.a_off + stages * C::kATileBytes;
+  L.sfw_off = L.abf_off + stages * C::kAbfBytes;
   L.sfa_off = L.sfw_off + stages * kSfTileBytes;
   const uint32_t end = L.sfa_off + stages * C::kSfaStageBytes;
   L.bar_off = end > static_cast<uint32_t>(C::kStagingBytes) ? end : C::kStagingBytes;
-  // barriers: full_tma[stages], full_a[stages], empty[stages], accum; then the
-  // tensor-memory address and the abort flag
-  L.total = L.bar_off + (3 * stages + 1) * 8 + 16;
+  // barriers: full_tma, full_abf, full_a, empty (one per stage each), accum;
+  // then the tensor-memory address and the abort flag
+  L.total = L.bar_off + (4 * stages + 1) * 8 + 16;
   return L;
 }
 
+// Byte offset of scale j (0..3) of row r in a 128-row x 4-scale chunk.
+__device__ __forceinline__ uint32_t sf_chunk_offset(int r) { return (r & 31) * 16 + ((r & 127) >> 5) * 4; }
+
 template <int BM, bool kFused>
-__global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
-    mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
-  using C = TileCfg<BM>;
+__global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
+    mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
+                      const GemmArgs args) {
+  using C = TileCfg<BM, kFused>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int stages = args.stages;
-  const SmemLayout L = smem_layout<BM>(stages);
+  const SmemLayout L = smem_layout<BM, kFused>(stages);
   auto full_tma = [&](int s) { return sbase + L.bar_off + 8u * s; };
-  auto full_a = [&](int s) { return sbase + L.bar_off + 8u * (stages + s); };
-  auto empty = [&](int s) { return sbase + L.bar_off + 8u * (2 * stages + s); };
-  const uint32_t accum_bar = sbase + L.bar_off + 8u * (3 * stages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.bar_off + 8 * (3 * stages + 1));
+  auto full_abf = [&](int s) { return sbase + L.bar_off + 8u * (stages + s); };
+  auto full_a = [&](int s) { return sbase + L.bar_off + 8u * (2 * stages + s); };
+  auto empty = [&](int s) { return sbase + L.bar_off + 8u * (3 * stages + s); };
+  const uint32_t accum_bar = sbase + L.bar_off + 8u * (4 * stages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.bar_off + 8 * (4 * stages + 1));
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int splits = args.splits;
   const uint32_t rank = splits > 1 ? cluster_ctarank() : 0u;
   const int n_tile = blockIdx.y, m_tile = blockIdx.z;
+  const int m_base = m_tile * BM;
+  const int m_valid = min(BM, args.M - m_base);
   const int kt_begin = static_cast<int>(rank) * args.kt_per_split;
   const int kt_end = min(args.k_tiles, kt_begin + args.kt_per_split);
   const int kt_count = max(0, kt_end - kt_begin);
@@ -104,6 +119,7 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_tma(s), 1);
+      mbar_init(full_abf(s), 1);
       mbar_init(full_a(s), C::kAThreads);
       mbar_init(empty(s), 1);
     }
@@ -111,7 +127,10 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
     *abort_flag = 0u;
     fence_mbar_init();
   }
-  if (warp == 0 && lane == 0) prefetch_tmap(&tmap_b);
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmap_b);
+    prefetch_tmap(&tmap_a);
+  }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
     tmem_relinquish();
@@ -122,10 +141,23 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t tmem_sf = tmem_base + BM;  // scale columns follow the accumulator
 
+  // The next call in the stream may start its own prologue now.  Everything
+  // below that reads data an earlier grid may write, or writes global memory,
+  // comes after grid_dependency_wait(); before it, only L2 prefetches.
+  grid_launch_dependents();
+
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      const uint64_t policy = policy_evict_first();  // weights are read once per call
+      for (int i = 0; i < kt_count; ++i) {
+        const int kt = kt_begin + i;
+        tma_prefetch_l2_2d(&tmap_b, kt * kTileKBytes, n_tile * kTileN);
+        bulk_prefetch_l2(args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes, kSfTileBytes);
+        tma_prefetch_l2_2d(&tmap_a, kFused ? kt * kTileK : kt * kTileKBytes, m_base);
+      }
+      grid_dependency_wait();
+      const uint64_t policy_b = policy_evict_first();  // weights: read once per call
+      const uint64_t policy_a = policy_evict_last();   // activations: shared by every N tile
       int issued = 0;
       for (int i = 0; i < kt_count; ++i) {
         const int s = i % stages, round = i / stages;
@@ -135,18 +167,26 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
         }
         if (*abort_flag) break;
         const int kt = kt_begin + i;
-        mbar_arrive_expect_tx(full_tma(s), C::kBTileBytes + kSfTileBytes);
-        tma_load_2d(sbase + s * C::kBTileBytes, &tmap_b, kt * kTileKBytes, n_tile * kTileN, full_tma(s),
-                    policy);
+        if constexpr (kFused) {
+          mbar_arrive_expect_tx(full_abf(s), C::kAbfBytes);
+          tma_load_2d(sbase + L.abf_off + s * C::kAbfBytes, &tmap_a, kt * kTileK, m_base, full_abf(s), policy_a);
+          mbar_arrive_expect_tx(full_tma(s), C::kBTileBytes + kSfTileBytes);
+        } else {
+          mbar_arrive_expect_tx(full_tma(s), C::kBTileBytes + kSfTileBytes + C::kATileBytes);
+          tma_load_2d(sbase + L.a_off + s * C::kATileBytes, &tmap_a, kt * kTileKBytes, m_base, full_tma(s),
+                      policy_a);
+        }
+        tma_load_2d(sbase + s * C::kBTileBytes, &tmap_b, kt * kTileKBytes, n_tile * kTileN, full_tma(s), policy_b);
         bulk_load(sbase + L.sfw_off + s * kSfTileBytes,
-                  args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes,
-                  kSfTileBytes, full_tma(s), policy);
+                  args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes, kSfTileBytes,
+                  full_tma(s), policy_b);
         issued = i + 1;
       }
       // Before the CTA can exit, every copy it issued must have landed.
       for (int s = 0; s < stages && s < issued; ++s) {
-        const int last = s + stages * ((issued - 1 - s) / stages);
-        if (!mbar_wait(full_tma(s), (last / stages) & 1, timeout)) report_error(args.err, kErrWaitDrain);
+        const uint32_t parity = ((s + stages * ((issued - 1 - s) / stages)) / stages) & 1;
+        if (!mbar_wait(full_tma(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
+        if (kFused && !mbar_wait(full_abf(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
       }
     }
     __syncwarp();
@@ -192,77 +232,74 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
   } else {
     // ------------------------------------------------------------------ activation producer
     const int tid = threadIdx.x - 64;
-    const int m_base = m_tile * BM;
-    for (int i = 0; i < kt_count; ++i) {
-      const int s = i % stages, round = i / stages;
-      if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
-        report_error(args.err, kErrWaitEmpty);
-        *abort_flag = 1u;
-      }
-      if (*abort_flag) break;
-      const int k0 = (kt_begin + i) * kTileK;
-      uint8_t* a_tile = smem + L.a_off + s * C::kATileBytes;
-      uint8_t* sfa = smem + L.sfa_off + s * C::kSfaStageBytes;
-      if constexpr (kFused) {
-        // 16-byte units: 32 per row of the tile (256 bf16), lanes 4b..4b+3 = block b
-        constexpr int kUnits = BM * 32 / C::kAThreads;
-        constexpr int kBatch = kUnits < 8 ? kUnits : 8;
-        const uint16_t* A = static_cast<const uint16_t*>(args.a);
-#pragma unroll
-        for (int t0 = 0; t0 < kUnits; t0 += kBatch) {
-          uint4 v[kBatch];
-#pragma unroll
-          for (int t = 0; t < kBatch; ++t) {
-            const int u = tid + (t0 + t) * C::kAThreads;
-            const int m = u >> 5, j = u & 31;
-            const int gm = m_base + m, gk = k0 + j * 8;
-            v[t] = make_uint4(0, 0, 0, 0);
-            if (gm < args.M && gk < args.K)
-              v[t] = __ldg(reinterpret_cast<const uint4*>(A + static_cast<int64_t>(gm) * args.lda + gk));
-          }
-#pragma unroll
-          for (int t = 0; t < kBatch; ++t) {
-            const int u = tid + (t0 + t) * C::kAThreads;
-            const int m = u >> 5, j = u & 31, b = j >> 2, q = j & 3;
-            uint32_t byte;
-            const uint32_t codes = quantize_quad(v[t], &byte);
-            *reinterpret_cast<uint32_t*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + q * 4) = codes;
-            if (q == 0) {
-              const int r = m & 127;
-              sfa[((b >> 2) * C::kRowChunks + (m >> 7)) * kSfChunkBytes + (r & 31) * 16 + (r >> 5) * 4 + (b & 3)] =
-                  static_cast<uint8_t>(byte);
-            }
-          }
+    grid_dependency_wait();  // the activation (and later C) may belong to the earlier grid
+    if constexpr (!kFused) {
+      // Pre-quantized activation: the codes arrive by TMA; place the natural
+      // [M, K/32] scales into the chunk layout, one row per thread.
+      const int64_t nblk = args.K / 32;
+      for (int i = 0; i < kt_count; ++i) {
+        const int s = i % stages, round = i / stages;
+        if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+          report_error(args.err, kErrWaitEmpty);
+          *abort_flag = 1u;
         }
-      } else {
-        // 16-byte units = one 32-element block of codes: 8 per row of the tile
-        constexpr int kUnits = BM * 8 / C::kAThreads;
-        const uint8_t* Aq = static_cast<const uint8_t*>(args.a);
-        const int64_t kh = args.K / 2, nblk = args.K / 32;
-        uint4 v[kUnits];
-        uint8_t sc[kUnits];
+        if (*abort_flag) break;
+        const int64_t j0 = static_cast<int64_t>(kt_begin + i) * 8;
+        uint8_t* sfa = smem + L.sfa_off + s * C::kSfaStageBytes;
+        for (int r = tid; r < m_valid; r += C::kAThreads) {
+          const uint8_t* src = args.a_scales + static_cast<int64_t>(m_base + r) * nblk + j0;
+          uint32_t w[2] = {0u, 0u};
 #pragma unroll
+          for (int b = 0; b < 8; ++b)
+            if (j0 + b < nblk) w[b >> 2] |= static_cast<uint32_t>(__ldg(src + b)) << (8 * (b & 3));
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            *reinterpret_cast<uint32_t*>(sfa + (c * C::kRowChunks + (r >> 7)) * kSfChunkBytes + sf_chunk_offset(r)) = w[c];
+        }
+        fence_proxy_async_smem();
+        mbar_arrive(full_a(s));
+      }
+    } else {
+      // Fused: quantize the staged bf16 tile.  16-byte units, 32 per row (256
+      // bf16); the 4 lanes of a quad share a 32-element block; rows past M are
+      // skipped (their output columns are never stored).
+      constexpr int kUnits = BM * 32 / C::kAThreads;
+      for (int i = 0; i < kt_count; ++i) {
+        const int s = i % stages, round = i / stages;
+        if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+          report_error(args.err, kErrWaitEmpty);
+          *abort_flag = 1u;
+        }
+        if (!*abort_flag && !mbar_wait(full_abf(s), round & 1, timeout)) {
+          report_error(args.err, kErrWaitTma);
+          *abort_flag = 1u;
+        }
+        if (*abort_flag) break;
+        const uint8_t* abf = smem + L.abf_off + s * C::kAbfBytes;
+        uint8_t* a_tile = smem + L.a_off + s * C::kATileBytes;
+        uint8_t* sfa = smem + L.sfa_off + s * C::kSfaStageBytes;
+#pragma unroll 4
         for (int t = 0; t < kUnits; ++t) {
           const int u = tid + t * C::kAThreads;
-          const int m = u >> 3, b = u & 7;
-          const int gm = m_base + m, gk = k0 + b * 32;
-          v[t] = make_uint4(0, 0, 0, 0);
-          sc[t] = 0;
-          if (gm < args.M && gk < args.K) {
-            v[t] = __ldg(reinterpret_cast<const uint4*>(Aq + gm * kh + gk / 2));
-            sc[t] = __ldg(args.a_scales + gm * nblk + gk / 32);
+          const int m = u >> 5, j = u & 31, b = j >> 2, q = j & 3;
+          if (m >= m_valid) break;  // warp-uniform: a warp's 32 units share one row
+          const uint4 v = *reinterpret_cast<const uint4*>(abf + m * (kTileK * 2) + j * 16);
+          uint32_t byte;
+          const uint32_t codes = quantize_quad(v, &byte);
+          *reinterpret_cast<uint32_t*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + q * 4) = codes;
+          // gather the scale bytes of blocks 4c..4c+3 (lanes 0, 4, 8, 12 / 16, 20, 24, 28) into one word
+          const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
+          const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 8);
+          const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 12);
+          if ((lane & 15) == 0) {
+            const uint32_t w = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
+            *reinterpret_cast<uint32_t*>(sfa + ((lane >> 4) * C::kRowChunks + (m >> 7)) * kSfChunkBytes +
+                                         sf_chunk_offset(m)) = w;
           }
         }
-#pragma unroll
-        for (int t = 0; t < kUnits; ++t) {
-          const int u = tid + t * C::kAThreads;
-          const int m = u >> 3, b = u & 7, r = m & 127;
-          *reinterpret_cast<uint4*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4)) = v[t];
-          sfa[((b >> 2) * C::kRowChunks + (m >> 7)) * kSfChunkBytes + (r & 31) * 16 + (r >> 5) * 4 + (b & 3)] = sc[t];
-        }
+        fence_proxy_async_smem();  // make the generic stores visible to tcgen05
+        mbar_arrive(full_a(s));
       }
-      fence_proxy_async_smem();  // make the generic stores visible to tcgen05
-      mbar_arrive(full_a(s));
     }
 
     // ------------------------------------------------------------------ epilogue: TMEM -> smem fp32
@@ -275,8 +312,9 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
     constexpr int kColGroups = C::kAWarps / 4;
     constexpr int kColsPerWarp = BM / kColGroups;
     const int col0 = ((warp - 2) >> 2) * kColsPerWarp;
+    const int col_end = min(col0 + kColsPerWarp, (m_valid + 15) & ~15);
 #pragma unroll 1
-    for (int c = col0; c < col0 + kColsPerWarp; c += 16) {
+    for (int c = col0; c < col_end; c += 16) {
       uint32_t r[16];
       if (have) {
         tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c, r);
@@ -300,7 +338,6 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
   if (warp >= 2) {
     // -------------------------------------------------------------- reduce the splits, store bf16
     const int tid = threadIdx.x - 64;
-    const int m_valid = min(BM, args.M - m_tile * BM);
     const int total = m_valid * (kTileN / 4);  // float4 vectors
     const int n_base = n_tile * kTileN;
     const bool vec_ok = (args.N % 4) == 0;
@@ -317,7 +354,7 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
           acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
         }
       }
-      const int64_t gm = static_cast<int64_t>(m_tile) * BM + m;
+      const int64_t gm = static_cast<int64_t>(m_base) + m;
       const int gn = n_base + n4 * 4;
       __nv_bfloat16* dst = args.c + gm * args.N + gn;
       if (vec_ok && gn + 3 < args.N) {
@@ -339,8 +376,8 @@ __global__ void __launch_bounds__(TileCfg<BM>::kThreads, 1)
 
 // ----------------------------------------------------------------------------- host side
 template <int BM, bool kFused>
-static cudaError_t launch_t(const CUtensorMap& tmap_b, const GemmArgs& args, const mxfp4_plan_t& plan,
-                            cudaStream_t s) {
+static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const GemmArgs& args,
+                            const mxfp4_plan_t& plan, bool programmatic, cudaStream_t s) {
   auto kernel = mxfp4_gemm_kernel<BM, kFused>;
   static int configured_device = -1;  // max dynamic smem set once per device
   int dev = 0;
@@ -356,35 +393,42 @@ static cudaError_t launch_t(const CUtensorMap& tmap_b, const GemmArgs& args, con
   cfg.blockDim = dim3(plan.threads, 1, 1);
   cfg.dynamicSmemBytes = plan.smem_bytes;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = plan.splits;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, tmap_b, args);
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, tmap_b, tmap_a, args);
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tmap_b, const GemmArgs& args, const mxfp4_plan_t& plan,
-                        bool fused, cudaStream_t s) {
+cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const GemmArgs& args,
+                        const mxfp4_plan_t& plan, bool fused, bool programmatic, cudaStream_t s) {
+#define MXFP4_LAUNCH(BM_)                                                                     \
+  case BM_:                                                                                   \
+    return fused ? launch_t<BM_, true>(tmap_b, tmap_a, args, plan, programmatic, s)           \
+                 : launch_t<BM_, false>(tmap_b, tmap_a, args, plan, programmatic, s);
   switch (plan.block_m) {
-    case 32: return fused ? launch_t<32, true>(tmap_b, args, plan, s) : launch_t<32, false>(tmap_b, args, plan, s);
-    case 64: return fused ? launch_t<64, true>(tmap_b, args, plan, s) : launch_t<64, false>(tmap_b, args, plan, s);
-    case 128: return fused ? launch_t<128, true>(tmap_b, args, plan, s) : launch_t<128, false>(tmap_b, args, plan, s);
-    case 256: return fused ? launch_t<256, true>(tmap_b, args, plan, s) : launch_t<256, false>(tmap_b, args, plan, s);
+    MXFP4_LAUNCH(32)
+    MXFP4_LAUNCH(64)
+    MXFP4_LAUNCH(128)
+    MXFP4_LAUNCH(256)
     default: return cudaErrorInvalidValue;
   }
+#undef MXFP4_LAUNCH
 }
 
 static int threads_for(int bm) { return bm >= 128 ? 64 + 256 : 64 + 128; }
 
-static SmemLayout layout_for(int bm, int stages) {
+static SmemLayout layout_for(int bm, bool fused, int stages) {
   switch (bm) {
-    case 32: return smem_layout<32>(stages);
-    case 64: return smem_layout<64>(stages);
-    case 128: return smem_layout<128>(stages);
-    default: return smem_layout<256>(stages);
+    case 32: return fused ? smem_layout<32, true>(stages) : smem_layout<32, false>(stages);
+    case 64: return fused ? smem_layout<64, true>(stages) : smem_layout<64, false>(stages);
+    case 128: return fused ? smem_layout<128, true>(stages) : smem_layout<128, false>(stages);
+    default: return fused ? smem_layout<256, true>(stages) : smem_layout<256, false>(stages);
   }
 }
 
@@ -398,7 +442,6 @@ static uint32_t pow2_at_least(uint32_t x) {
 
 bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                  mxfp4_plan_t* p) {
-  (void)fused;
   if (p->block_m != 32 && p->block_m != 64 && p->block_m != 128 && p->block_m != 256) return false;
   const int64_t k_tiles = ceil_div(K, kTileK);
   if (p->splits < 1 || p->splits > kMaxSplits || p->splits > k_tiles) return false;
@@ -415,7 +458,7 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
   const uint32_t tcols = pow2_at_least(p->block_m + p->stages * sf_cols_for(p->block_m));
   if (tcols > 512) return false;
   p->tmem_cols = static_cast<int32_t>(tcols);
-  const SmemLayout L = layout_for(p->block_m, p->stages);
+  const SmemLayout L = layout_for(p->block_m, fused, p->stages);
   int64_t smem = static_cast<int64_t>(L.total) + 1024;  // + alignment slack
   // Tensor-memory allocation blocks while the SM's 512 columns are taken, and
   // a blocked CTA of one cluster could then wait on a CTA of another cluster
@@ -446,10 +489,10 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
   const int64_t per = ceil_div(k_tiles, splits);
   splits = ceil_div(k_tiles, per);  // no empty split
   p->splits = static_cast<int32_t>(splits);
-  p->stages = 0;  // finish_plan: min(per, 8)
+  p->stages = 0;  // finish_plan: min(per, 6)
   if (!finish_plan(M, N, K, fused, prop, p)) {
     // fall back to fewer stages (shared memory) -- still the same kernel
-    for (int st = 7; st >= 1; --st) {
+    for (int st = 5; st >= 1; --st) {
       mxfp4_plan_t q = *p;
       q.stages = st;
       if (finish_plan(M, N, K, fused, prop, &q)) {
@@ -457,6 +500,7 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
         return;
       }
     }
+    *p = mxfp4_plan_t{};
   }
 }
 

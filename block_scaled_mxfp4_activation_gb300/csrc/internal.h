@@ -73,8 +73,8 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
                  mxfp4_plan_t* plan);
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                   mxfp4_plan_t* plan);
-cudaError_t launch_gemm(const CUtensorMap& tmap_b, const GemmArgs& args, const mxfp4_plan_t& plan,
-                        bool fused, cudaStream_t s);
+cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const GemmArgs& args,
+                        const mxfp4_plan_t& plan, bool fused, bool programmatic, cudaStream_t s);
 
 cudaError_t read_device_error(cudaStream_t s, uint32_t* code, bool reset);
 // Address of the device error word on the current device (nullptr on failure).

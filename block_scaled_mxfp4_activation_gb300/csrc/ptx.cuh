@@ -131,6 +131,30 @@ __device__ __forceinline__ uint64_t policy_evict_last() {
   return p;
 }
 
+// Prefetch of a 2-D tensor box / a byte range into L2 (no shared-memory write,
+// no completion tracking).  L2 is the GPU's point of coherence, so prefetching
+// data that an earlier grid is still writing cannot make a later read stale.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* tm, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global [%0, {%1, %2}];" ::"l"(tm), "r"(x), "r"(y)
+               : "memory");
+}
+
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// ----------------------------------------------------------------------------- grid dependencies
+// Programmatic dependent launch: let the next grid in the stream start its
+// prologue now / wait until the previous grid has completed and its memory
+// operations are visible (a no-op when launched without the attribute).
+__device__ __forceinline__ void grid_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ----------------------------------------------------------------------------- tcgen05
 // Allocates `ncols` tensor-memory columns (a power of two >= 32); the whole
 // warp executes it and the address lands in shared memory at `dst`.

@@ -152,6 +152,16 @@ mxfp4_status_t mxfp4_device_error(mxfp4_stream_t stream, int reset, uint32_t* co
  * this call (default 1e9; 0 restores the default). */
 mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns);
 
+/* Programmatic dependent launch of the GEMM entries (default on).  When on, a
+ * GEMM launched right after another kernel on the same stream may start
+ * before that kernel ends: until the earlier grid has completed it only sets
+ * up shared and tensor memory and prefetches its weight and activation bytes
+ * into L2 (L2 is coherent, so this never reads stale data); every read of
+ * data the earlier grid may write, and every global write, waits for it.
+ * Back-to-back calls then overlap one call's set-up and DRAM latency with the
+ * previous call's tail.  Off: every launch waits for the previous one. */
+mxfp4_status_t mxfp4_set_programmatic_launch(int enable);
+
 /* Diagnostic: launches one tiny kernel whose wait can never complete (an
  * mbarrier nothing arrives on) and that therefore gives up after the current
  * wait limit and sets the device error word.  Lets a caller check that bounded
