@@ -37,9 +37,10 @@ STATUS_NAMES = {
 
 
 class MXFP4Error(RuntimeError):
-    def __init__(self, status: int, what: str):
+    def __init__(self, status: int, what: str, detail: str = ""):
         self.status = status
-        super().__init__(f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})")
+        msg = f"{what}: {STATUS_NAMES.get(status, status)} ({status_string(status)})"
+        super().__init__(msg + (f": {detail}" if detail else ""))
 
 
 class Plan(ctypes.Structure):
@@ -86,6 +87,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             "mxfp4_set_wait_timeout_ns": ([ctypes.c_uint64], st),
             "mxfp4_diag_wait_timeout": ([S], st),
             "mxfp4_set_programmatic_launch": ([ctypes.c_int], st),
+            "mxfp4_last_error_string": ([], ctypes.c_char_p),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -112,9 +114,11 @@ def _ptr(t: torch.Tensor | None):
 
 
 def _call(name: str, *args):
-    status = getattr(load_library(), name)(*args)
+    lib = load_library()
+    status = getattr(lib, name)(*args)
     if status != MXFP4_OK:
-        raise MXFP4Error(status, name)
+        detail = lib.mxfp4_last_error_string().decode() if status == 5 else ""
+        raise MXFP4Error(status, name, detail)
 
 
 def _need(t: torch.Tensor, dtype: torch.dtype, what: str):
@@ -261,9 +265,11 @@ def set_wait_timeout_ns(ns: int) -> None:
     _call("mxfp4_set_wait_timeout_ns", int(ns))
 
 
-def set_programmatic_launch(enable: bool) -> None:
-    """Programmatic dependent launch of the GEMM entries (default on)."""
-    _call("mxfp4_set_programmatic_launch", int(bool(enable)))
+def set_programmatic_launch(mode: int) -> None:
+    """Overlap of a GEMM call with the kernel before it: 0 none, 1 set-up and
+    L2 prefetch only, 2 (default) also the weights into shared memory; see
+    mxfp4_set_programmatic_launch in include/mxfp4.h."""
+    _call("mxfp4_set_programmatic_launch", int(mode))
 
 
 def diag_wait_timeout(stream=None) -> None:

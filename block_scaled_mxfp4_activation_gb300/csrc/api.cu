@@ -3,7 +3,10 @@
 #include <cudaTypedefs.h>
 
 #include <atomic>
+#include <cstdio>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "internal.h"
 
@@ -11,7 +14,20 @@ namespace mxfp4 {
 namespace {
 
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
-std::atomic<int> g_programmatic{1};
+std::atomic<int> g_programmatic{2};
+
+// The CUDA error behind the last MXFP4_ERR_CUDA status of this thread.
+thread_local char g_last_error[256] = "";
+
+mxfp4_status_t cuda_failure(const char* what, cudaError_t e) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+  return MXFP4_ERR_CUDA;
+}
+
+mxfp4_status_t failure(const char* what) {
+  snprintf(g_last_error, sizeof(g_last_error), "%s", what);
+  return MXFP4_ERR_CUDA;
+}
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -25,8 +41,9 @@ const DeviceInfo* current_device(mxfp4_status_t* st) {
   static DeviceInfo info[64];
   static std::once_flag once[64];
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
-    *st = MXFP4_ERR_CUDA;
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= 64) {
+    *st = e != cudaSuccess ? cuda_failure("cudaGetDevice", e) : failure("device index out of range");
     return nullptr;
   }
   std::call_once(once[dev], [dev]() {
@@ -101,6 +118,29 @@ bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, boo
   return r == CUDA_SUCCESS;
 }
 
+// The default plan per (device, M, N, K, fused), computed once: the plan
+// search queries cluster occupancy, which is too slow for every call.
+void cached_default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
+                         mxfp4_plan_t* plan) {
+  static std::mutex mu;
+  static std::map<std::tuple<int, int64_t, int64_t, int64_t, bool>, mxfp4_plan_t> cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const auto key = std::make_tuple(dev, M, N, K, fused);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *plan = it->second;
+      return;
+    }
+  }
+  default_plan(M, N, K, fused, prop, plan);
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = *plan;
+}
+
 constexpr int64_t kMaxDim = int64_t(1) << 30;
 
 mxfp4_status_t check_mnk(int64_t M, int64_t N, int64_t K) {
@@ -133,12 +173,13 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
     plan.stages = user_plan->stages;
     if (!finish_plan(M, N, K, fused, dev->prop, &plan)) return MXFP4_ERR_INVALID_ARG;
   } else {
-    default_plan(M, N, K, fused, dev->prop, &plan);
+    cached_default_plan(M, N, K, fused, dev->prop, &plan);
     if (plan.threads == 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   }
   CUtensorMap map, amap;
-  if (!encode_weight_map(bpacked, N, K, &map)) return MXFP4_ERR_CUDA;
-  if (!encode_activation_map(a, M, K, fused ? lda : K / 2, fused, plan.block_m, &amap)) return MXFP4_ERR_CUDA;
+  if (!encode_weight_map(bpacked, N, K, &map)) return failure("cuTensorMapEncodeTiled (weights)");
+  if (!encode_activation_map(a, M, K, fused ? lda : K / 2, fused, plan.block_m, &amap))
+    return failure("cuTensorMapEncodeTiled (activation)");
   GemmArgs g{};
   g.a = a;
   g.a_scales = static_cast<const uint8_t*>(as);
@@ -155,11 +196,19 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   g.stages = plan.stages;
   g.tmem_cols = static_cast<uint32_t>(plan.tmem_cols);
   g.timeout_ns = g_timeout_ns.load();
+  const GemmLayout GL = gemm_layout(plan.block_m, plan.stages, plan.splits, fused, M);
+  g.a_off = GL.a_off;
+  g.abf_off = GL.abf_off;
+  g.sfw_off = GL.sfw_off;
+  g.sfa_off = GL.sfa_off;
+  g.stg_off = GL.stg_off;
+  g.bar_off = GL.bar_off;
+  g.stg_blocks = GL.stg_blocks;
+  g.weights_early = g_programmatic.load() >= 2 ? 1 : 0;
   g.err = device_error_word();
-  if (g.err == nullptr) return MXFP4_ERR_CUDA;
-  return launch_gemm(map, amap, g, plan, fused, g_programmatic.load() != 0, stream) == cudaSuccess
-             ? MXFP4_OK
-             : MXFP4_ERR_CUDA;
+  if (g.err == nullptr) return failure("cudaGetSymbolAddress (device error word)");
+  const cudaError_t e = launch_gemm(map, amap, g, plan, fused, g_programmatic.load() != 0, stream);
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("GEMM launch", e);
 }
 
 }  // namespace
@@ -177,9 +226,8 @@ mxfp4_status_t mxfp4_quantize(const void* A, int64_t M, int64_t K, int64_t lda, 
   if (!aligned16(A) || !aligned16(Aq) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
   mxfp4_status_t st;
   if (current_device(&st) == nullptr) return st;
-  return launch_quantize(A, M, K, lda, Aq, As, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MXFP4_OK
-             : MXFP4_ERR_CUDA;
+  const cudaError_t e = launch_quantize(A, M, K, lda, Aq, As, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("quantize launch", e);
 }
 
 size_t mxfp4_packed_weight_bytes(int64_t N, int64_t K) {
@@ -195,9 +243,8 @@ mxfp4_status_t mxfp4_pack_weights(const void* Bq, const void* Bs, int64_t N, int
   if (!aligned16(Bq) || !aligned16(Bpacked)) return MXFP4_ERR_MISALIGNED;
   mxfp4_status_t st;
   if (current_device(&st) == nullptr) return st;
-  return launch_pack_weights(Bq, Bs, N, K, Bpacked, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MXFP4_OK
-             : MXFP4_ERR_CUDA;
+  const cudaError_t e = launch_pack_weights(Bq, Bs, N, K, Bpacked, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("weight packing launch", e);
 }
 
 mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, void* Bq, void* Bs,
@@ -208,9 +255,8 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
   if (!aligned16(Bq) || !aligned16(Bpacked)) return MXFP4_ERR_MISALIGNED;
   mxfp4_status_t st;
   if (current_device(&st) == nullptr) return st;
-  return launch_unpack_weights(Bpacked, N, K, Bq, Bs, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MXFP4_OK
-             : MXFP4_ERR_CUDA;
+  const cudaError_t e = launch_unpack_weights(Bpacked, N, K, Bq, Bs, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("weight unpacking launch", e);
 }
 
 size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -240,7 +286,7 @@ mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4
   if (st != MXFP4_OK) return st;
   const DeviceInfo* dev = current_device(&st);
   if (dev == nullptr) return st;
-  default_plan(M, N, K, fused != 0, dev->prop, plan);
+  cached_default_plan(M, N, K, fused != 0, dev->prop, plan);
   return plan->threads == 0 ? MXFP4_ERR_UNSUPPORTED_SHAPE : MXFP4_OK;
 }
 
@@ -270,27 +316,29 @@ mxfp4_status_t mxfp4_device_error(mxfp4_stream_t stream, int reset, uint32_t* co
   if (code == nullptr) return MXFP4_ERR_INVALID_ARG;
   mxfp4_status_t st;
   if (current_device(&st) == nullptr) return st;
-  if (read_device_error(reinterpret_cast<cudaStream_t>(stream), code, reset != 0) != cudaSuccess)
-    return MXFP4_ERR_CUDA;
+  const cudaError_t e = read_device_error(reinterpret_cast<cudaStream_t>(stream), code, reset != 0);
+  if (e != cudaSuccess) return cuda_failure("reading the device error word", e);
   return *code != 0 ? MXFP4_ERR_DEVICE_TIMEOUT : MXFP4_OK;
 }
+
+const char* mxfp4_last_error_string(void) { return g_last_error; }
 
 mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns) {
   g_timeout_ns.store(ns == 0 ? 1000000000ull : ns);
   return MXFP4_OK;
 }
 
-mxfp4_status_t mxfp4_set_programmatic_launch(int enable) {
-  g_programmatic.store(enable != 0 ? 1 : 0);
+mxfp4_status_t mxfp4_set_programmatic_launch(int mode) {
+  if (mode < 0 || mode > 2) return MXFP4_ERR_INVALID_ARG;
+  g_programmatic.store(mode);
   return MXFP4_OK;
 }
 
 mxfp4_status_t mxfp4_diag_wait_timeout(mxfp4_stream_t stream) {
   mxfp4_status_t st;
   if (current_device(&st) == nullptr) return st;
-  return launch_diag_wait(g_timeout_ns.load(), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
-             ? MXFP4_OK
-             : MXFP4_ERR_CUDA;
+  const cudaError_t e = launch_diag_wait(g_timeout_ns.load(), reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("diagnostic launch", e);
 }
 
 }  // extern "C"

@@ -43,14 +43,17 @@ struct TileCfg {
   static constexpr int kATileBytes = BM * kTileKBytes;             // activation codes
   static constexpr int kAbfBytes = kFused ? BM * kTileK * 2 : 0;   // bf16 activation staging
   static constexpr int kSfaStageBytes = 2 * kRowChunks * kSfChunkBytes;
-  static constexpr int kStageBytes = kBTileBytes + kATileBytes + kAbfBytes + kSfTileBytes + kSfaStageBytes;
-  static constexpr int kAWarps = BM >= 128 ? 8 : 4;                // producer / epilogue warps
+  static constexpr int kAWarps = 8;                                // producer / epilogue warps
   static constexpr int kAThreads = kAWarps * 32;
   static constexpr int kThreads = 64 + kAThreads;
   static constexpr int kSfCols = 8 + 8 * kRowChunks;               // TMEM scale columns per stage
-  static constexpr int kStagingBytes = BM * kTileN * 4;            // fp32 partial tile
   static_assert(BM % 32 == 0 && BM <= 256, "block_m must be 32, 64, 128 or 256");
 };
+
+// The accumulator tile (128 weight rows x BM activation rows) is reduced over
+// K splits in blocks of 32 weight rows (one TMEM lane quarter) x 16 activation
+// rows (one tcgen05.ld): 2 KB of fp32 each.
+constexpr int kBlockBytes = 32 * 16 * 4;
 
 // Instruction descriptor of kind::mxf4 (E2M1 x E2M1, UE8M0 scales, fp32
 // accumulate): A/B formats at bits 7-9 / 10-12 (E2M1 = 1), both K-major, N >> 3
@@ -61,27 +64,6 @@ template <int BM>
 __device__ __forceinline__ uint32_t mxf4_idesc(uint32_t scale_id) {
   return (1u << 7) | (1u << 10) | (static_cast<uint32_t>(BM >> 3) << 17) | (1u << 23) |
          (static_cast<uint32_t>(kTileN >> 4) << 24) | (scale_id << 29) | (scale_id << 4);
-}
-
-// Shared-memory layout of one CTA (offsets from a 1024-byte aligned base).
-struct SmemLayout {
-  uint32_t a_off, abf_off, sfw_off, sfa_off, bar_off, total;
-};
-
-template <int BM, bool kFused>
-__host__ __device__ inline SmemLayout smem_layout(int stages) {
-  using C = TileCfg<BM, kFused>;
-  SmemLayout L;
-  L.a_off = stages * C::kBTileBytes;
-  L.abf_off = L.a_off + stages * C::kATileBytes;
-  L.sfw_off = L.abf_off + stages * C::kAbfBytes;
-  L.sfa_off = L.sfw_off + stages * kSfTileBytes;
-  const uint32_t end = L.sfa_off + stages * C::kSfaStageBytes;
-  L.bar_off = end > static_cast<uint32_t>(C::kStagingBytes) ? end : C::kStagingBytes;
-  // barriers: full_tma, full_abf, full_a, empty (one per stage each), accum;
-  // then the tensor-memory address and the abort flag
-  L.total = L.bar_off + (4 * stages + 1) * 8 + 16;
-  return L;
 }
 
 // Byte offset of scale j (0..3) of row r in a 128-row x 4-scale chunk.
@@ -96,13 +78,12 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int stages = args.stages;
-  const SmemLayout L = smem_layout<BM, kFused>(stages);
-  auto full_tma = [&](int s) { return sbase + L.bar_off + 8u * s; };
-  auto full_abf = [&](int s) { return sbase + L.bar_off + 8u * (stages + s); };
-  auto full_a = [&](int s) { return sbase + L.bar_off + 8u * (2 * stages + s); };
-  auto empty = [&](int s) { return sbase + L.bar_off + 8u * (3 * stages + s); };
-  const uint32_t accum_bar = sbase + L.bar_off + 8u * (4 * stages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L.bar_off + 8 * (4 * stages + 1));
+  auto full_w = [&](int s) { return sbase + args.bar_off + 8u * s; };                 // weight codes + scales
+  auto full_in = [&](int s) { return sbase + args.bar_off + 8u * (stages + s); };     // activation tile (TMA)
+  auto full_a = [&](int s) { return sbase + args.bar_off + 8u * (2 * stages + s); };  // operand ready for the MMA
+  auto empty = [&](int s) { return sbase + args.bar_off + 8u * (3 * stages + s); };   // stage consumed
+  const uint32_t accum_bar = sbase + args.bar_off + 8u * (4 * stages);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + args.bar_off + 8 * (4 * stages + 1));
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -118,8 +99,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
-      mbar_init(full_tma(s), 1);
-      mbar_init(full_abf(s), 1);
+      mbar_init(full_w(s), 1);
+      mbar_init(full_in(s), 1);
       mbar_init(full_a(s), C::kAThreads);
       mbar_init(empty(s), 1);
     }
@@ -141,52 +122,70 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   const uint32_t tmem_base = *tmem_slot;
   const uint32_t tmem_sf = tmem_base + BM;  // scale columns follow the accumulator
 
-  // The next call in the stream may start its own prologue now.  Everything
-  // below that reads data an earlier grid may write, or writes global memory,
-  // comes after grid_dependency_wait(); before it, only L2 prefetches.
+  // The next call in the stream may start its own prologue now.  Reads of data
+  // an earlier grid may write (the activation) and every global write come
+  // after grid_dependency_wait(); before it, only the weights (read-only for
+  // the lifetime of the call, by contract) and L2 prefetches.
   grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
     if (lane == 0) {
-      for (int i = 0; i < kt_count; ++i) {
-        const int kt = kt_begin + i;
-        tma_prefetch_l2_2d(&tmap_b, kt * kTileKBytes, n_tile * kTileN);
-        bulk_prefetch_l2(args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes, kSfTileBytes);
-        tma_prefetch_l2_2d(&tmap_a, kFused ? kt * kTileK : kt * kTileKBytes, m_base);
-      }
-      grid_dependency_wait();
       const uint64_t policy_b = policy_evict_first();  // weights: read once per call
       const uint64_t policy_a = policy_evict_last();   // activations: shared by every N tile
-      int issued = 0;
-      for (int i = 0; i < kt_count; ++i) {
+      const int pre = min(stages, kt_count);
+      auto issue_w = [&](int i) {
+        const int s = i % stages, kt = kt_begin + i;
+        mbar_arrive_expect_tx(full_w(s), C::kBTileBytes + kSfTileBytes);
+        tma_load_2d(sbase + s * C::kBTileBytes, &tmap_b, kt * kTileKBytes, n_tile * kTileN, full_w(s), policy_b);
+        bulk_load(sbase + args.sfw_off + s * kSfTileBytes,
+                  args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes, kSfTileBytes,
+                  full_w(s), policy_b);
+      };
+      auto issue_a = [&](int i) {
+        const int s = i % stages, kt = kt_begin + i;
+        if constexpr (kFused) {
+          mbar_arrive_expect_tx(full_in(s), C::kAbfBytes);
+          tma_load_2d(sbase + args.abf_off + s * C::kAbfBytes, &tmap_a, kt * kTileK, m_base, full_in(s), policy_a);
+        } else {
+          mbar_arrive_expect_tx(full_in(s), C::kATileBytes);
+          tma_load_2d(sbase + args.a_off + s * C::kATileBytes, &tmap_a, kt * kTileKBytes, m_base, full_in(s),
+                      policy_a);
+        }
+      };
+      if (args.weights_early) {
+        for (int i = 0; i < pre; ++i) issue_w(i);
+      } else {
+        for (int i = 0; i < kt_count; ++i) {
+          const int kt = kt_begin + i;
+          tma_prefetch_l2_2d(&tmap_b, kt * kTileKBytes, n_tile * kTileN);
+          bulk_prefetch_l2(args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes,
+                           kSfTileBytes);
+        }
+      }
+      for (int i = 0; i < kt_count; ++i)
+        tma_prefetch_l2_2d(&tmap_a, kFused ? (kt_begin + i) * kTileK : (kt_begin + i) * kTileKBytes, m_base);
+      grid_dependency_wait();
+      if (!args.weights_early)
+        for (int i = 0; i < pre; ++i) issue_w(i);
+      for (int i = 0; i < pre; ++i) issue_a(i);
+      int issued = pre;
+      for (int i = pre; i < kt_count; ++i) {
         const int s = i % stages, round = i / stages;
-        if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+        if (!mbar_wait(empty(s), (round - 1) & 1, timeout)) {
           report_error(args.err, kErrWaitEmpty);
           *abort_flag = 1u;
         }
         if (*abort_flag) break;
-        const int kt = kt_begin + i;
-        if constexpr (kFused) {
-          mbar_arrive_expect_tx(full_abf(s), C::kAbfBytes);
-          tma_load_2d(sbase + L.abf_off + s * C::kAbfBytes, &tmap_a, kt * kTileK, m_base, full_abf(s), policy_a);
-          mbar_arrive_expect_tx(full_tma(s), C::kBTileBytes + kSfTileBytes);
-        } else {
-          mbar_arrive_expect_tx(full_tma(s), C::kBTileBytes + kSfTileBytes + C::kATileBytes);
-          tma_load_2d(sbase + L.a_off + s * C::kATileBytes, &tmap_a, kt * kTileKBytes, m_base, full_tma(s),
-                      policy_a);
-        }
-        tma_load_2d(sbase + s * C::kBTileBytes, &tmap_b, kt * kTileKBytes, n_tile * kTileN, full_tma(s), policy_b);
-        bulk_load(sbase + L.sfw_off + s * kSfTileBytes,
-                  args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes, kSfTileBytes,
-                  full_tma(s), policy_b);
+        issue_w(i);
+        issue_a(i);
         issued = i + 1;
       }
       // Before the CTA can exit, every copy it issued must have landed.
       for (int s = 0; s < stages && s < issued; ++s) {
         const uint32_t parity = ((s + stages * ((issued - 1 - s) / stages)) / stages) & 1;
-        if (!mbar_wait(full_tma(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
-        if (kFused && !mbar_wait(full_abf(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
+        if (!mbar_wait(full_w(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
+        if (!mbar_wait(full_in(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
       }
     }
     __syncwarp();
@@ -195,26 +194,30 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     if (lane == 0) {
       for (int i = 0; i < kt_count; ++i) {
         const int s = i % stages, round = i / stages;
-        bool ok = mbar_wait(full_tma(s), round & 1, timeout);
-        if (!ok) report_error(args.err, kErrWaitTma);
-        ok = ok && mbar_wait(full_a(s), round & 1, timeout);
-        if (!ok) {
-          report_error(args.err, kErrWaitA);
+        if (!mbar_wait(full_w(s), round & 1, timeout)) {
+          report_error(args.err, kErrWaitTma);
           *abort_flag = 1u;
         }
         if (*abort_flag) break;
         tc_fence_after_sync();
         const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
         const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
-        const uint32_t sfw_s = sbase + L.sfw_off + s * kSfTileBytes;
-        const uint32_t sfa_s = sbase + L.sfa_off + s * C::kSfaStageBytes;
+        const uint32_t sfw_s = sbase + args.sfw_off + s * kSfTileBytes;
+        const uint32_t sfa_s = sbase + args.sfa_off + s * C::kSfaStageBytes;
+        // the weight scales can move to tensor memory while the activation is still being prepared
 #pragma unroll
         for (int c = 0; c < 2; ++c) tmem_cp_32x128b_warpx4(sfw_t + 4 * c, smem_desc(sfw_s + c * kSfChunkBytes, 128, 128, 0));
+        if (!mbar_wait(full_a(s), round & 1, timeout)) {
+          report_error(args.err, kErrWaitA);
+          *abort_flag = 1u;
+        }
+        if (*abort_flag) break;
+        tc_fence_after_sync();
 #pragma unroll
         for (int c = 0; c < 2 * C::kRowChunks; ++c)
           tmem_cp_32x128b_warpx4(sfa_t + 4 * c, smem_desc(sfa_s + c * kSfChunkBytes, 128, 128, 0));
         const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
-        const uint64_t b_desc = smem_desc(sbase + L.a_off + s * C::kATileBytes, 16, 1024, 2);
+        const uint64_t b_desc = smem_desc(sbase + args.a_off + s * C::kATileBytes, 16, 1024, 2);
         const int k0 = (kt_begin + i) * kTileK;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
@@ -232,103 +235,111 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   } else {
     // ------------------------------------------------------------------ activation producer
     const int tid = threadIdx.x - 64;
-    grid_dependency_wait();  // the activation (and later C) may belong to the earlier grid
-    if constexpr (!kFused) {
-      // Pre-quantized activation: the codes arrive by TMA; place the natural
-      // [M, K/32] scales into the chunk layout, one row per thread.
-      const int64_t nblk = args.K / 32;
-      for (int i = 0; i < kt_count; ++i) {
-        const int s = i % stages, round = i / stages;
-        if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
-          report_error(args.err, kErrWaitEmpty);
-          *abort_flag = 1u;
+    grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
+    constexpr int kUnits = BM * 32 / C::kAThreads;     // fused: 16-byte bf16 units per thread and K tile
+    constexpr int kRowsPerPass = C::kAThreads / 32;   // unit t of a warp covers row warp_row + t * kRowsPerPass
+    constexpr int kBatch = kUnits < 4 ? kUnits : 4;
+    const int warp_row = tid >> 5;
+    const int t_end = m_valid > warp_row ? min(kUnits, (m_valid - warp_row + kRowsPerPass - 1) / kRowsPerPass) : 0;
+    const int b = lane >> 2, q = lane & 3;
+    const int64_t nblk = args.K / 32;
+    for (int i = 0; i < kt_count; ++i) {
+      const int s = i % stages, round = i / stages;
+      if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+        report_error(args.err, kErrWaitEmpty);
+        *abort_flag = 1u;
+      }
+      if (!*abort_flag && !mbar_wait(full_in(s), round & 1, timeout)) {
+        report_error(args.err, kErrWaitTma);
+        *abort_flag = 1u;
+      }
+      if (*abort_flag) break;
+      uint8_t* a_tile = smem + args.a_off + s * C::kATileBytes;
+      uint8_t* sfa = smem + args.sfa_off + s * C::kSfaStageBytes;
+      if constexpr (kFused) {
+        // Quantize the staged bf16 tile: 16-byte units, 32 per row (256 bf16);
+        // the 4 lanes of a quad share a 32-element block; rows past M are
+        // skipped (their output columns are never stored).
+        const uint8_t* abf = smem + args.abf_off + s * C::kAbfBytes;
+        for (int t0 = 0; t0 < t_end; t0 += kBatch) {
+          uint4 v[kBatch];  // all loads of a batch first, then the independent chains
+#pragma unroll
+          for (int e = 0; e < kBatch; ++e) {
+            const int m = warp_row + (t0 + e) * kRowsPerPass;
+            v[e] = (t0 + e < t_end) ? *reinterpret_cast<const uint4*>(abf + m * (kTileK * 2) + lane * 16)
+                                    : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+          for (int e = 0; e < kBatch; ++e) {
+            const int m = warp_row + (t0 + e) * kRowsPerPass;
+            uint32_t byte;
+            const uint32_t codes = quantize_quad(v[e], &byte);
+            if (t0 + e < t_end) {
+              *reinterpret_cast<uint32_t*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + q * 4) = codes;
+              if (q == 0)
+                sfa[((b >> 2) * C::kRowChunks + (m >> 7)) * kSfChunkBytes + sf_chunk_offset(m) + (b & 3)] =
+                    static_cast<uint8_t>(byte);
+            }
+          }
         }
-        if (*abort_flag) break;
+      } else {
+        // Pre-quantized activation: the codes arrived by TMA; place the
+        // natural [M, K/32] scales into the chunk layout, one row per thread.
         const int64_t j0 = static_cast<int64_t>(kt_begin + i) * 8;
-        uint8_t* sfa = smem + L.sfa_off + s * C::kSfaStageBytes;
         for (int r = tid; r < m_valid; r += C::kAThreads) {
           const uint8_t* src = args.a_scales + static_cast<int64_t>(m_base + r) * nblk + j0;
           uint32_t w[2] = {0u, 0u};
 #pragma unroll
-          for (int b = 0; b < 8; ++b)
-            if (j0 + b < nblk) w[b >> 2] |= static_cast<uint32_t>(__ldg(src + b)) << (8 * (b & 3));
+          for (int jb = 0; jb < 8; ++jb)
+            if (j0 + jb < nblk) w[jb >> 2] |= static_cast<uint32_t>(__ldg(src + jb)) << (8 * (jb & 3));
 #pragma unroll
           for (int c = 0; c < 2; ++c)
             *reinterpret_cast<uint32_t*>(sfa + (c * C::kRowChunks + (r >> 7)) * kSfChunkBytes + sf_chunk_offset(r)) = w[c];
         }
-        fence_proxy_async_smem();
-        mbar_arrive(full_a(s));
       }
-    } else {
-      // Fused: quantize the staged bf16 tile.  16-byte units, 32 per row (256
-      // bf16); the 4 lanes of a quad share a 32-element block; rows past M are
-      // skipped (their output columns are never stored).
-      constexpr int kUnits = BM * 32 / C::kAThreads;
-      for (int i = 0; i < kt_count; ++i) {
-        const int s = i % stages, round = i / stages;
-        if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
-          report_error(args.err, kErrWaitEmpty);
-          *abort_flag = 1u;
-        }
-        if (!*abort_flag && !mbar_wait(full_abf(s), round & 1, timeout)) {
-          report_error(args.err, kErrWaitTma);
-          *abort_flag = 1u;
-        }
-        if (*abort_flag) break;
-        const uint8_t* abf = smem + L.abf_off + s * C::kAbfBytes;
-        uint8_t* a_tile = smem + L.a_off + s * C::kATileBytes;
-        uint8_t* sfa = smem + L.sfa_off + s * C::kSfaStageBytes;
-#pragma unroll 4
-        for (int t = 0; t < kUnits; ++t) {
-          const int u = tid + t * C::kAThreads;
-          const int m = u >> 5, j = u & 31, b = j >> 2, q = j & 3;
-          if (m >= m_valid) break;  // warp-uniform: a warp's 32 units share one row
-          const uint4 v = *reinterpret_cast<const uint4*>(abf + m * (kTileK * 2) + j * 16);
-          uint32_t byte;
-          const uint32_t codes = quantize_quad(v, &byte);
-          *reinterpret_cast<uint32_t*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + q * 4) = codes;
-          // gather the scale bytes of blocks 4c..4c+3 (lanes 0, 4, 8, 12 / 16, 20, 24, 28) into one word
-          const uint32_t b1 = __shfl_down_sync(0xFFFFFFFFu, byte, 4);
-          const uint32_t b2 = __shfl_down_sync(0xFFFFFFFFu, byte, 8);
-          const uint32_t b3 = __shfl_down_sync(0xFFFFFFFFu, byte, 12);
-          if ((lane & 15) == 0) {
-            const uint32_t w = byte | (b1 << 8) | (b2 << 16) | (b3 << 24);
-            *reinterpret_cast<uint32_t*>(sfa + ((lane >> 4) * C::kRowChunks + (m >> 7)) * kSfChunkBytes +
-                                         sf_chunk_offset(m)) = w;
-          }
-        }
-        fence_proxy_async_smem();  // make the generic stores visible to tcgen05
-        mbar_arrive(full_a(s));
-      }
+      fence_proxy_async_smem();  // make the generic stores visible to tcgen05
+      mbar_arrive(full_a(s));
     }
 
-    // ------------------------------------------------------------------ epilogue: TMEM -> smem fp32
-    bool ok = mbar_wait(accum_bar, 0, timeout);
+    // ------------------------------------------------------------------ epilogue: push partial blocks
+    // Block (chunk c of 16 activation rows, lane quarter qr) goes to cluster
+    // rank (4c + qr) % splits, into that CTA's slot [this rank][(4c + qr) / splits].
+    // The staging area is separate from the stage buffers, so a peer still
+    // running its MMAs is never disturbed.
+    const bool ok = mbar_wait(accum_bar, 0, timeout);
     if (!ok) report_error(args.err, kErrWaitAccum);
     tc_fence_after_sync();
     const bool have = ok && kt_count > 0 && !*abort_flag;
-    float* staging = reinterpret_cast<float*>(smem);  // [BM][128], reuses the stage buffers
-    const int quarter = warp & 3;                     // TMEM lanes this warp may read
-    constexpr int kColGroups = C::kAWarps / 4;
-    constexpr int kColsPerWarp = BM / kColGroups;
-    const int col0 = ((warp - 2) >> 2) * kColsPerWarp;
-    const int col_end = min(col0 + kColsPerWarp, (m_valid + 15) & ~15);
+    const int qr = warp & 3;           // TMEM lanes this warp may read
+    const int h = (warp - 2) >> 2;     // which half of the column chunks
+    const int chunks = (m_valid + 15) >> 4;
 #pragma unroll 1
-    for (int c = col0; c < col_end; c += 16) {
+    for (int c = h; c < chunks; c += 2) {
       uint32_t r[16];
       if (have) {
-        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c, r);
+        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(qr * 32) << 16) + c * 16, r);
         tmem_ld_wait();
       } else {
 #pragma unroll
         for (int e = 0; e < 16; ++e) r[e] = 0u;
       }
+      const int bi = 4 * c + qr;
+      const uint32_t owner = static_cast<uint32_t>(bi % splits);
+      const uint32_t dst = sbase + args.stg_off +
+                           (static_cast<uint32_t>(rank) * args.stg_blocks + bi / splits) * kBlockBytes + lane * 4;
+      if (splits == 1) {
 #pragma unroll
-      for (int e = 0; e < 16; ++e) staging[(c + e) * kTileN + quarter * 32 + lane] = __uint_as_float(r[e]);
+        for (int e = 0; e < 16; ++e)
+          *reinterpret_cast<float*>(smem + (dst - sbase) + e * 128) = __uint_as_float(r[e]);
+      } else {
+        const uint32_t cdst = map_to_rank(dst, owner);
+#pragma unroll
+        for (int e = 0; e < 16; ++e) st_cluster_f32(cdst + e * 128, __uint_as_float(r[e]));
+      }
     }
   }
 
-  // ---------------------------------------------------------------------- partial tiles visible
+  // ---------------------------------------------------------------------- every partial delivered
   tc_fence_before_sync();
   if (splits > 1) cluster_sync_all(); else __syncthreads();
   if (warp == 1) {
@@ -336,42 +347,43 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     tmem_dealloc(tmem_base, args.tmem_cols);
   }
   if (warp >= 2) {
-    // -------------------------------------------------------------- reduce the splits, store bf16
+    // ------------------------------------------------ sum the owned blocks over the splits, store bf16
+    // Only local shared memory is read from here on, so no CTA waits for its
+    // peers before exiting.
     const int tid = threadIdx.x - 64;
-    const int total = m_valid * (kTileN / 4);  // float4 vectors
+    const int valid_blocks = 4 * ((m_valid + 15) >> 4);
+    const int mine = (valid_blocks - static_cast<int>(rank) + splits - 1) / splits;
     const int n_base = n_tile * kTileN;
     const bool vec_ok = (args.N % 4) == 0;
-    for (int v = static_cast<int>(rank) * C::kAThreads + tid; v < total; v += splits * C::kAThreads) {
-      const int m = v >> 5, n4 = v & 31;
-      const uint32_t off = m * (kTileN * 4) + n4 * 16;
-      float4 acc;
-      if (splits == 1) {
-        acc = *reinterpret_cast<const float4*>(smem + off);
-      } else {
-        acc = ld_cluster_f4(map_to_rank(sbase + off, 0));
-        for (int src = 1; src < splits; ++src) {
-          const float4 p = ld_cluster_f4(map_to_rank(sbase + off, src));
-          acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
-        }
+    const uint8_t* stg = smem + args.stg_off;
+    for (int it = tid; it < mine * 128; it += C::kAThreads) {
+      const int lb = it >> 7, w = it & 127, row = w >> 3, c4 = w & 7;
+      const int bi = lb * splits + static_cast<int>(rank);
+      const int m = (bi >> 2) * 16 + row;
+      if (m >= m_valid) continue;
+      const uint32_t off = lb * kBlockBytes + row * 128 + c4 * 16;
+      float4 acc = *reinterpret_cast<const float4*>(stg + off);
+      for (int src = 1; src < splits; ++src) {
+        const float4 p = *reinterpret_cast<const float4*>(stg + src * args.stg_blocks * kBlockBytes + off);
+        acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
       }
       const int64_t gm = static_cast<int64_t>(m_base) + m;
-      const int gn = n_base + n4 * 4;
+      const int gn = n_base + (bi & 3) * 32 + c4 * 4;
       __nv_bfloat16* dst = args.c + gm * args.N + gn;
       if (vec_ok && gn + 3 < args.N) {
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
-        uint2 w;
-        w.x = *reinterpret_cast<const uint32_t*>(&lo);
-        w.y = *reinterpret_cast<const uint32_t*>(&hi);
-        *reinterpret_cast<uint2*>(dst) = w;
+        uint2 wv;
+        wv.x = *reinterpret_cast<const uint32_t*>(&lo);
+        wv.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(dst) = wv;
       } else {
         const float e[4] = {acc.x, acc.y, acc.z, acc.w};
-        for (int q = 0; q < 4; ++q)
-          if (gn + q < args.N) dst[q] = __float2bfloat16_rn(e[q]);
+        for (int qq = 0; qq < 4; ++qq)
+          if (gn + qq < args.N) dst[qq] = __float2bfloat16_rn(e[qq]);
       }
     }
   }
-  if (splits > 1) cluster_sync_all();  // peers may still read this CTA's partial tile
 }
 
 // ----------------------------------------------------------------------------- host side
@@ -421,16 +433,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, co
 #undef MXFP4_LAUNCH
 }
 
-static int threads_for(int bm) { return bm >= 128 ? 64 + 256 : 64 + 128; }
-
-static SmemLayout layout_for(int bm, bool fused, int stages) {
-  switch (bm) {
-    case 32: return fused ? smem_layout<32, true>(stages) : smem_layout<32, false>(stages);
-    case 64: return fused ? smem_layout<64, true>(stages) : smem_layout<64, false>(stages);
-    case 128: return fused ? smem_layout<128, true>(stages) : smem_layout<128, false>(stages);
-    default: return fused ? smem_layout<256, true>(stages) : smem_layout<256, false>(stages);
-  }
-}
+static int threads_for(int) { return 64 + 256; }
 
 static int sf_cols_for(int bm) { return 8 + 8 * (bm > 128 ? 2 : 1); }
 
@@ -438,6 +441,22 @@ static uint32_t pow2_at_least(uint32_t x) {
   uint32_t p = 32;
   while (p < x) p <<= 1;
   return p;
+}
+
+GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M) {
+  GemmLayout L;
+  const uint32_t st = static_cast<uint32_t>(stages), bm = static_cast<uint32_t>(block_m);
+  L.a_off = st * kTileN * kTileKBytes;
+  L.abf_off = L.a_off + st * bm * kTileKBytes;
+  L.sfw_off = L.abf_off + (fused ? st * bm * kTileK * 2 : 0u);
+  L.sfa_off = L.sfw_off + st * kSfTileBytes;
+  L.stg_off = L.sfa_off + st * (bm > 128 ? 2u : 1u) * 2u * kSfChunkBytes;
+  const int64_t rows = M < block_m ? M : block_m;
+  const int blocks = static_cast<int>(4 * ceil_div(rows, 16));
+  L.stg_blocks = static_cast<int32_t>(ceil_div(blocks, splits));
+  L.bar_off = L.stg_off + static_cast<uint32_t>(splits * L.stg_blocks) * kBlockBytes;
+  L.total = L.bar_off + (4 * st + 1) * 8 + 16;
+  return L;
 }
 
 bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
@@ -458,7 +477,7 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
   const uint32_t tcols = pow2_at_least(p->block_m + p->stages * sf_cols_for(p->block_m));
   if (tcols > 512) return false;
   p->tmem_cols = static_cast<int32_t>(tcols);
-  const SmemLayout L = layout_for(p->block_m, fused, p->stages);
+  const GemmLayout L = gemm_layout(p->block_m, p->stages, p->splits, fused, M);
   int64_t smem = static_cast<int64_t>(L.total) + 1024;  // + alignment slack
   // Tensor-memory allocation blocks while the SM's 512 columns are taken, and
   // a blocked CTA of one cluster could then wait on a CTA of another cluster
@@ -476,31 +495,87 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
   return true;
 }
 
+template <int BM, bool kFused>
+static int active_clusters_t(const mxfp4_plan_t& p) {
+  auto kernel = mxfp4_gemm_kernel<BM, kFused>;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) return 0;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.grid_x, p.grid_y, p.grid_z);
+  cfg.blockDim = dim3(p.threads, 1, 1);
+  cfg.dynamicSmemBytes = p.smem_bytes;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = p.splits;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+    cudaGetLastError();  // clear the sticky-free error so later calls are unaffected
+    return 0;
+  }
+  return n;
+}
+
+// How many clusters of this plan can be resident at once on the device.
+static int active_clusters(const mxfp4_plan_t& p, bool fused) {
+#define MXFP4_OCC(BM_) \
+  case BM_: return fused ? active_clusters_t<BM_, true>(p) : active_clusters_t<BM_, false>(p);
+  switch (p.block_m) {
+    MXFP4_OCC(32)
+    MXFP4_OCC(64)
+    MXFP4_OCC(128)
+    MXFP4_OCC(256)
+    default: return 0;
+  }
+#undef MXFP4_OCC
+}
+
+// The default plan.  Every call is latency-bound, so the plan maximises the
+// work in flight: as many CTAs as can be resident at once, up to two per SM
+// (two CTAs per SM keep twice the bytes in flight and quantize twice the
+// activation in parallel), all in a single wave.  Candidates: block_m from the
+// smallest tile that holds M (capped at 256) down to a quarter of it; every
+// split count that leaves no split empty; one or two stages (the ring wraps
+// when a split has more K tiles), or every K tile of the split when that
+// still fits.  Ties prefer the larger block_m (fewer re-reads of the weights),
+// then the larger stage count, then fewer splits.
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                   mxfp4_plan_t* p) {
   *p = mxfp4_plan_t{};
-  p->block_m = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  const int bm0 = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   const int64_t k_tiles = ceil_div(K, kTileK);
-  const int64_t tiles = ceil_div(N, kTileN) * ceil_div(M, p->block_m);
-  int64_t splits = prop.multiProcessorCount / (tiles > 0 ? tiles : 1);
-  if (splits < 1) splits = 1;
-  if (splits > kMaxSplits) splits = kMaxSplits;
-  if (splits > k_tiles) splits = k_tiles;
-  const int64_t per = ceil_div(k_tiles, splits);
-  splits = ceil_div(k_tiles, per);  // no empty split
-  p->splits = static_cast<int32_t>(splits);
-  p->stages = 0;  // finish_plan: min(per, 6)
-  if (!finish_plan(M, N, K, fused, prop, p)) {
-    // fall back to fewer stages (shared memory) -- still the same kernel
-    for (int st = 5; st >= 1; --st) {
-      mxfp4_plan_t q = *p;
-      q.stages = st;
-      if (finish_plan(M, N, K, fused, prop, &q)) {
-        *p = q;
-        return;
+  const int64_t cap = 2 * static_cast<int64_t>(prop.multiProcessorCount);
+  int64_t best[5] = {-1, 0, 0, 0, 0};
+  for (int bm = bm0; bm >= 32 && bm * 4 >= bm0; bm /= 2) {
+    for (int64_t splits = 1; splits <= kMaxSplits && splits <= k_tiles; ++splits) {
+      const int64_t per = ceil_div(k_tiles, splits);
+      if ((splits - 1) * per >= k_tiles) continue;  // an empty split
+      for (int64_t st : {int64_t(1), int64_t(2), per}) {
+        if (st > per || st > 6 || (st == per && per <= 2 && st != 1 && st != 2)) continue;
+        mxfp4_plan_t q{};
+        q.block_m = bm;
+        q.splits = static_cast<int32_t>(splits);
+        q.stages = static_cast<int32_t>(st);
+        if (!finish_plan(M, N, K, fused, prop, &q) || q.stages != st) continue;
+        const int64_t clusters = static_cast<int64_t>(q.grid_y) * q.grid_z;
+        const int64_t ctas = clusters * splits;
+        const int64_t one_wave = clusters <= active_clusters(q, fused) ? 1 : 0;
+        const int64_t score[5] = {one_wave, ctas <= cap ? ctas : -ctas, bm, st, -splits};
+        bool better = false;
+        for (int i = 0; i < 5; ++i) {
+          if (score[i] != best[i]) {
+            better = score[i] > best[i];
+            break;
+          }
+        }
+        if (better) {
+          for (int i = 0; i < 5; ++i) best[i] = score[i];
+          *p = q;
+        }
       }
     }
-    *p = mxfp4_plan_t{};
   }
 }
 

@@ -8,7 +8,7 @@
 #include <cstddef>
 #include <cstdint>
 
-#include "../../include/mxfp4.h"
+#include "mxfp4.h"
 
 namespace mxfp4 {
 
@@ -56,7 +56,21 @@ struct GemmArgs {
   uint32_t tmem_cols;
   uint64_t timeout_ns;
   uint32_t* err;            // device error word
+  int32_t weights_early;    // issue the weight loads before waiting on the previous grid
+  // shared-memory layout (byte offsets from the 1024-aligned base), see smem_layout()
+  uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off;
+  int32_t stg_blocks;       // 32 x 16 partial blocks each CTA may receive from one split
 };
+
+// Shared-memory layout of one GEMM CTA (byte offsets from a 1024-aligned base):
+// weight code tiles, activation code tiles, bf16 activation staging (fused),
+// weight scales, activation scales (one of each per stage), the split-K
+// staging slots ([splits][stg_blocks] blocks of 2 KB), then the mbarriers.
+struct GemmLayout {
+  uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off, total;
+  int32_t stg_blocks;
+};
+GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M);
 
 // Launchers (return a CUDA error code; arguments are validated by the caller).
 cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,

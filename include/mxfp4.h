@@ -143,6 +143,10 @@ mxfp4_status_t mxfp4_gemm_with_plan(const void* A_or_Aq, int64_t lda, const void
  * ------------------------------------------------------------------------- */
 const char* mxfp4_status_string(mxfp4_status_t status);
 
+/* The CUDA call and error behind the last MXFP4_ERR_CUDA status returned on
+ * the calling thread ("" if none); valid until the thread's next call. */
+const char* mxfp4_last_error_string(void);
+
 /* Synchronises `stream`, then reads the device error word (0 = no device-side
  * failure since the last reset) into *code and, if reset != 0, clears it.
  * Returns MXFP4_ERR_DEVICE_TIMEOUT if the word is non-zero, else MXFP4_OK. */
@@ -152,15 +156,23 @@ mxfp4_status_t mxfp4_device_error(mxfp4_stream_t stream, int reset, uint32_t* co
  * this call (default 1e9; 0 restores the default). */
 mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns);
 
-/* Programmatic dependent launch of the GEMM entries (default on).  When on, a
- * GEMM launched right after another kernel on the same stream may start
- * before that kernel ends: until the earlier grid has completed it only sets
- * up shared and tensor memory and prefetches its weight and activation bytes
- * into L2 (L2 is coherent, so this never reads stale data); every read of
- * data the earlier grid may write, and every global write, waits for it.
- * Back-to-back calls then overlap one call's set-up and DRAM latency with the
- * previous call's tail.  Off: every launch waits for the previous one. */
-mxfp4_status_t mxfp4_set_programmatic_launch(int enable);
+/* How a GEMM call may overlap the kernel before it on the same stream
+ * (programmatic dependent launch):
+ *   0  no overlap: the GEMM starts after the previous kernel has finished;
+ *   1  the GEMM may start early, but until the previous kernel has completed
+ *      it only sets up and prefetches its weight and activation bytes into L2
+ *      (L2 is coherent, so this never reads stale data);
+ *   2  (default) as 1, and the weight codes and scales are also loaded into
+ *      shared memory before the previous kernel has completed.  Contract: the
+ *      packed weight buffer is not written by the kernel that immediately
+ *      precedes the GEMM on its stream (weights are read-only parameters; none
+ *      of this library's kernels writes a weight buffer it is not given as an
+ *      output, and a kernel that does not use programmatic launch has always
+ *      completed before the GEMM starts).
+ * In every mode the activation is read, and C written, only after the
+ * previous kernel has completed.  Back-to-back calls then overlap one call's
+ * set-up and weight streaming with the previous call's tail. */
+mxfp4_status_t mxfp4_set_programmatic_launch(int mode);
 
 /* Diagnostic: launches one tiny kernel whose wait can never complete (an
  * mbarrier nothing arrives on) and that therefore gives up after the current
