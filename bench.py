@@ -154,12 +154,15 @@ class Problem:
         A_dev = A.to(device)
         self.A = [A_dev] + [A_dev.clone() for _ in range(self.copies - 1)]
         self.C = [torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device) for _ in range(self.copies)]
+        # one workspace for every call: calls on a stream are ordered, and the
+        # quantize pass of a call waits for the previous GEMM before writing it
+        self.ws = torch.empty(max(mx.workspace_bytes(w.M, w.N, w.K), 1), dtype=torch.uint8, device=device)
         self.rotating_bytes = per_copy * self.copies
         self.l2 = l2
 
     def call(self, i: int):
         j = i % self.copies
-        self.mx.quant_gemm(self.A[j], self.W[j], out=self.C[j])
+        self.mx.quant_gemm(self.A[j], self.W[j], out=self.C[j], workspace=self.ws)
 
     def graph(self, n: int, stream: torch.cuda.Stream, rotate: bool = True) -> torch.cuda.CUDAGraph:
         g = torch.cuda.CUDAGraph()

@@ -46,7 +46,7 @@ class MXFP4Error(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "splits", "stages", "k_tiles_per_split", "grid_x", "grid_y", "grid_z", "threads",
-        "smem_bytes", "tmem_cols")]
+        "smem_bytes", "tmem_cols", "two_pass")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -210,8 +210,13 @@ def gemm(Aq: torch.Tensor, As: torch.Tensor, W: PackedWeight, out: torch.Tensor 
     return out
 
 
-def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """The fused layer: bf16 A [M, K] -> quantize in-kernel -> x packed W -> bf16 C [M, N]."""
+def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """The fused layer: bf16 A [M, K] -> quantized -> x packed W -> bf16 C [M, N].
+
+    `workspace` (uint8 CUDA tensor) lets large-M calls take the two-pass route;
+    when None, one of workspace_bytes(M, N, K) bytes is taken from torch's
+    allocator (none for small M).  Pass an explicit one to reuse it."""
     W = _weight(W)
     _need(A, torch.bfloat16, "A")
     if A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
@@ -219,7 +224,12 @@ def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
     M = A.shape[0]
     if out is None:
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
-    _call("mxfp4_quant_gemm", _ptr(A), A.stride(0), _ptr(W.data), _ptr(out), M, W.N, W.K, None, 0,
+    if workspace is None:
+        nbytes = workspace_bytes(M, W.N, W.K)
+        if nbytes:
+            workspace = torch.empty(nbytes, dtype=torch.uint8, device=A.device)
+    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel()) if workspace is not None else (None, 0)
+    _call("mxfp4_quant_gemm", _ptr(A), A.stride(0), _ptr(W.data), _ptr(out), M, W.N, W.K, ws_ptr, ws_bytes,
           _stream(stream))
     return out
 

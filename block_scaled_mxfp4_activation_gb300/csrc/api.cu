@@ -94,8 +94,14 @@ bool encode_weight_map(const void* bpacked, int64_t N, int64_t K, CUtensorMap* m
 // memory), or codes [M, K/2] with 128-byte x block_m boxes and the 128-byte
 // swizzle (landing directly in the MMA operand layout).  Rows past M and
 // columns past K read as zero.
+int activation_box_rows(int64_t M, int block_m) {
+  const int64_t r = (M + 7) / 8 * 8;
+  return static_cast<int>(r < block_m ? r : block_m);
+}
+
 bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, bool fused, int block_m,
                            CUtensorMap* map) {
+  const int rows = activation_box_rows(M, block_m);
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return false;
   cuuint32_t elem_strides[2] = {1, 1};
@@ -103,14 +109,14 @@ bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, boo
   if (fused) {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * 2)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(block_m)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(rows)};
     r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims, strides, box, elem_strides,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   } else {
     cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M)};
     cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKBytes), static_cast<cuuint32_t>(block_m)};
+    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKBytes), static_cast<cuuint32_t>(rows)};
     r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a), dims, strides, box, elem_strides,
                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -139,6 +145,18 @@ void cached_default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cuda
   std::lock_guard<std::mutex> lock(mu);
   if (cache.size() > 4096) cache.clear();
   cache[key] = *plan;
+}
+
+size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// The fused entry quantizes A once into a workspace and runs the GEMM on
+// codes when M is large enough that re-reading bf16 A in every N tile costs
+// more than the extra launch (measured on GB300: from M = 64 on).
+bool two_pass_wanted(int64_t M) { return M >= 64; }
+
+size_t two_pass_workspace(int64_t M, int64_t K) {
+  return align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2)) +
+         align256(static_cast<size_t>(M) * static_cast<size_t>(K / 32));
 }
 
 constexpr int64_t kMaxDim = int64_t(1) << 30;
@@ -204,6 +222,7 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   g.stg_off = GL.stg_off;
   g.bar_off = GL.bar_off;
   g.stg_blocks = GL.stg_blocks;
+  g.a_box_rows = activation_box_rows(M, plan.block_m);
   g.weights_early = g_programmatic.load() >= 2 ? 1 : 0;
   g.err = device_error_word();
   if (g.err == nullptr) return failure("cudaGetSymbolAddress (device error word)");
@@ -226,7 +245,8 @@ mxfp4_status_t mxfp4_quantize(const void* A, int64_t M, int64_t K, int64_t lda, 
   if (!aligned16(A) || !aligned16(Aq) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
   mxfp4_status_t st;
   if (current_device(&st) == nullptr) return st;
-  const cudaError_t e = launch_quantize(A, M, K, lda, Aq, As, reinterpret_cast<cudaStream_t>(stream));
+  const cudaError_t e =
+      launch_quantize(A, M, K, lda, Aq, As, g_programmatic.load() != 0, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("quantize launch", e);
 }
 
@@ -260,24 +280,37 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
 }
 
 size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-  (void)M;
-  (void)N;
-  (void)K;
-  return 0;  // K splits are reduced on chip, through cluster shared memory
+  if (check_mnk(M, N, K) != MXFP4_OK) return 0;
+  return two_pass_wanted(M) ? two_pass_workspace(M, K) : 0;
 }
 
 mxfp4_status_t mxfp4_gemm(const void* Aq, const void* As, const void* Bpacked, void* C, int64_t M,
                           int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
   (void)ws;
-  if (ws_bytes < mxfp4_workspace_bytes(M, N, K)) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+  (void)ws_bytes;  // the pre-quantized GEMM needs no scratch
   return run_gemm(Aq, K / 2, As, Bpacked, C, M, N, K, false, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
-  (void)ws;
-  if (ws_bytes < mxfp4_workspace_bytes(M, N, K)) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
-  return run_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, reinterpret_cast<cudaStream_t>(stream));
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mxfp4_status_t st = check_mnk(M, N, K);
+  if (st != MXFP4_OK) return st;
+  if (two_pass_wanted(M) && ws != nullptr && ws_bytes >= two_pass_workspace(M, K) && aligned16(ws)) {
+    // validate everything the GEMM checks before anything is launched
+    if (A == nullptr || Bpacked == nullptr || C == nullptr) return MXFP4_ERR_INVALID_ARG;
+    if (lda < K) return MXFP4_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(Bpacked) || !aligned16(C) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
+    if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    // Two passes: quantize A once into the workspace, then the GEMM on codes
+    // (the fused kernel would re-read the 4x larger bf16 A in every N tile).
+    uint8_t* Aq = static_cast<uint8_t*>(ws);
+    uint8_t* As = Aq + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
+    st = mxfp4_quantize(A, M, K, lda, Aq, As, stream);
+    if (st != MXFP4_OK) return st;
+    return run_gemm(Aq, K / 2, As, Bpacked, C, M, N, K, false, nullptr, s);
+  }
+  return run_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, s);
 }
 
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan) {
@@ -286,7 +319,9 @@ mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4
   if (st != MXFP4_OK) return st;
   const DeviceInfo* dev = current_device(&st);
   if (dev == nullptr) return st;
-  cached_default_plan(M, N, K, fused != 0, dev->prop, plan);
+  const bool two_pass = fused != 0 && two_pass_wanted(M);
+  cached_default_plan(M, N, K, fused != 0 && !two_pass, dev->prop, plan);
+  plan->two_pass = two_pass ? 1 : 0;
   return plan->threads == 0 ? MXFP4_ERR_UNSUPPORTED_SHAPE : MXFP4_OK;
 }
 

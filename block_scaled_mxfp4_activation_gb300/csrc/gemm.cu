@@ -145,10 +145,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
       auto issue_a = [&](int i) {
         const int s = i % stages, kt = kt_begin + i;
         if constexpr (kFused) {
-          mbar_arrive_expect_tx(full_in(s), C::kAbfBytes);
+          mbar_arrive_expect_tx(full_in(s), args.a_box_rows * kTileK * 2);
           tma_load_2d(sbase + args.abf_off + s * C::kAbfBytes, &tmap_a, kt * kTileK, m_base, full_in(s), policy_a);
         } else {
-          mbar_arrive_expect_tx(full_in(s), C::kATileBytes);
+          mbar_arrive_expect_tx(full_in(s), args.a_box_rows * kTileKBytes);
           tma_load_2d(sbase + args.a_off + s * C::kATileBytes, &tmap_a, kt * kTileKBytes, m_base, full_in(s),
                       policy_a);
         }
@@ -243,6 +243,27 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     const int t_end = m_valid > warp_row ? min(kUnits, (m_valid - warp_row + kRowsPerPass - 1) / kRowsPerPass) : 0;
     const int b = lane >> 2, q = lane & 3;
     const int64_t nblk = args.K / 32;
+    // unfused: the 8 scale bytes of row `tid` for K tile i (one row per thread;
+    // block_m <= 256 = the producer thread count)
+    auto load_scales = [&](int i, uint32_t& w0, uint32_t& w1) {
+      const int64_t j0 = static_cast<int64_t>(kt_begin + i) * 8;
+      const uint8_t* src = args.a_scales + static_cast<int64_t>(m_base + tid) * nblk + j0;
+      uint32_t w[2] = {0u, 0u};
+#pragma unroll
+      for (int jb = 0; jb < 8; ++jb)
+        if (j0 + jb < nblk) w[jb >> 2] |= static_cast<uint32_t>(__ldg(src + jb)) << (8 * (jb & 3));
+      w0 = w[0];
+      w1 = w[1];
+    };
+    constexpr int kPreK = kFused ? 1 : 8;
+    uint32_t sc_pre[kPreK][2];
+    if constexpr (!kFused) {
+      if (tid < m_valid) {
+#pragma unroll
+        for (int i = 0; i < kPreK; ++i)
+          if (i < kt_count) load_scales(i, sc_pre[i][0], sc_pre[i][1]);
+      }
+    }
     for (int i = 0; i < kt_count; ++i) {
       const int s = i % stages, round = i / stages;
       if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
@@ -284,17 +305,24 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
         }
       } else {
         // Pre-quantized activation: the codes arrived by TMA; place the
-        // natural [M, K/32] scales into the chunk layout, one row per thread.
-        const int64_t j0 = static_cast<int64_t>(kt_begin + i) * 8;
-        for (int r = tid; r < m_valid; r += C::kAThreads) {
-          const uint8_t* src = args.a_scales + static_cast<int64_t>(m_base + r) * nblk + j0;
-          uint32_t w[2] = {0u, 0u};
+        // natural [M, K/32] scales into the chunk layout, one row per thread
+        // (loaded for the first kPreK tiles before the loop, see below).
+        if (tid < m_valid) {
+          uint32_t w0, w1;
+          if (i < kPreK) {
+            w0 = w1 = 0u;
 #pragma unroll
-          for (int jb = 0; jb < 8; ++jb)
-            if (j0 + jb < nblk) w[jb >> 2] |= static_cast<uint32_t>(__ldg(src + jb)) << (8 * (jb & 3));
-#pragma unroll
-          for (int c = 0; c < 2; ++c)
-            *reinterpret_cast<uint32_t*>(sfa + (c * C::kRowChunks + (r >> 7)) * kSfChunkBytes + sf_chunk_offset(r)) = w[c];
+            for (int pk = 0; pk < kPreK; ++pk)  // register select (no dynamic indexing)
+              if (pk == i) {
+                w0 = sc_pre[pk][0];
+                w1 = sc_pre[pk][1];
+              }
+          } else {
+            load_scales(i, w0, w1);
+          }
+          const int r = tid;
+          *reinterpret_cast<uint32_t*>(sfa + (0 * C::kRowChunks + (r >> 7)) * kSfChunkBytes + sf_chunk_offset(r)) = w0;
+          *reinterpret_cast<uint32_t*>(sfa + (1 * C::kRowChunks + (r >> 7)) * kSfChunkBytes + sf_chunk_offset(r)) = w1;
         }
       }
       fence_proxy_async_smem();  // make the generic stores visible to tcgen05

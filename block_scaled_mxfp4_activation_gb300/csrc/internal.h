@@ -60,6 +60,7 @@ struct GemmArgs {
   // shared-memory layout (byte offsets from the 1024-aligned base), see smem_layout()
   uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off;
   int32_t stg_blocks;       // 32 x 16 partial blocks each CTA may receive from one split
+  int32_t a_box_rows;       // rows of one activation TMA box: min(block_m, roundup(M, 8))
 };
 
 // Shared-memory layout of one GEMM CTA (byte offsets from a 1024-aligned base):
@@ -74,7 +75,7 @@ GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t 
 
 // Launchers (return a CUDA error code; arguments are validated by the caller).
 cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
-                            cudaStream_t s);
+                            bool programmatic, cudaStream_t s);
 cudaError_t launch_pack_weights(const void* Bq, const void* Bs, int64_t N, int64_t K, void* Bp,
                                 cudaStream_t s);
 cudaError_t launch_unpack_weights(const void* Bp, int64_t N, int64_t K, void* Bq, void* Bs,

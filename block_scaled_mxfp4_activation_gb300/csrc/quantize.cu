@@ -35,8 +35,15 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   const bool valid = unit < M * units_per_row;
   const int64_t row = valid ? unit / units_per_row : 0;
   const int64_t j = valid ? unit - row * units_per_row : 0;
+  const uint16_t* src = A + row * lda + j * 8;
+  // Under programmatic launch the next kernel may start its prologue now; this
+  // one touches A and its outputs only once the previous grid has completed
+  // (the outputs may still be read by it), after an L2 prefetch of its line.
+  grid_launch_dependents();
+  if (valid && (j & 7) == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+  grid_dependency_wait();
   uint4 v = make_uint4(0, 0, 0, 0);
-  if (valid) v = __ldg(reinterpret_cast<const uint4*>(A + row * lda + j * 8));
+  if (valid) v = __ldg(reinterpret_cast<const uint4*>(src));
   uint32_t byte;
   const uint32_t codes = quantize_quad(v, &byte);  // every lane takes part in the shuffles
   if (valid) {
@@ -46,13 +53,20 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
 }
 
 cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
-                            cudaStream_t s) {
+                            bool programmatic, cudaStream_t s) {
   const int64_t units = M * (K / 8);
   const int threads = 256;
-  const int64_t blocks = ceil_div(units, threads);
-  quantize_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-      static_cast<const uint16_t*>(A), M, K, lda, static_cast<uint8_t*>(Aq), static_cast<uint8_t*>(As));
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(units, threads)), 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, quantize_kernel, static_cast<const uint16_t*>(A), M, K, lda,
+                            static_cast<uint8_t*>(Aq), static_cast<uint8_t*>(As));
 }
 
 // ----------------------------------------------------------------------------- weight relayout

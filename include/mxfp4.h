@@ -61,6 +61,9 @@ typedef struct {
   int32_t threads;    /* threads per CTA */
   int32_t smem_bytes; /* dynamic shared memory per CTA */
   int32_t tmem_cols;  /* tensor-memory columns allocated per CTA */
+  int32_t two_pass;   /* mxfp4_gemm_plan, fused entry: 1 if, given mxfp4_workspace_bytes() of
+                         workspace, it quantizes A into the workspace and runs the GEMM on
+                         codes (this plan then describes that GEMM) */
 } mxfp4_plan_t;
 
 /* ---------------------------------------------------------------------------
@@ -112,17 +115,28 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
  *   A        device, bf16 [M, lda]; lda % 8 == 0 (fused entry only)
  *   Bpacked  device, the output of mxfp4_pack_weights for the same N, K
  *   C        device, bf16 [M, N] row-major, fully overwritten
- *   ws, ws_bytes  scratch; the current plans need none (NULL, 0 is valid);
- *            mxfp4_workspace_bytes() gives the requirement.
+ *   ws, ws_bytes  device scratch, optional (NULL, 0 is always valid).
+ *            mxfp4_gemm never uses it.  mxfp4_quant_gemm uses it when M >= 64
+ *            and ws_bytes >= mxfp4_workspace_bytes(M, N, K) (16-byte aligned):
+ *            it then quantizes A into the workspace with mxfp4_quantize and
+ *            runs the GEMM on the codes -- two launches that overlap, and
+ *            faster than the single fused kernel once M is large, because the
+ *            fused kernel re-reads the bf16 activation in every 128-row weight
+ *            tile.  Without it, the single fused kernel runs.  The workspace
+ *            is overwritten; calls that share one must be ordered.
  * M, N >= 1.  Returns MXFP4_OK or an error status (nothing launched).
  * ------------------------------------------------------------------------- */
+/* Workspace that lets mxfp4_quant_gemm take its two-pass route (0 when the
+ * single fused kernel is best, or for invalid sizes): M*K/2 + M*K/32 bytes,
+ * each part rounded up to 256. */
 size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K);
 
 mxfp4_status_t mxfp4_gemm(const void* Aq, const void* As, const void* Bpacked, void* C, int64_t M,
                           int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
 
 /* The fused entry: quantizes A inside the GEMM kernel (no global Aq/As), with
- * the same rule and bit-identical codes as mxfp4_quantize. */
+ * the same rule and bit-identical codes as mxfp4_quantize (or, given a
+ * workspace for M >= 64, in a separate pass; see ws above). */
 mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes,
                                 mxfp4_stream_t stream);
@@ -169,6 +183,8 @@ mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns);
  *      of this library's kernels writes a weight buffer it is not given as an
  *      output, and a kernel that does not use programmatic launch has always
  *      completed before the GEMM starts).
+ * mxfp4_quantize follows modes 1 and 2 likewise: it may start early, but reads
+ * A and writes its outputs only after the previous kernel has completed.
  * In every mode the activation is read, and C written, only after the
  * previous kernel has completed.  Back-to-back calls then overlap one call's
  * set-up and weight streaming with the previous call's tail. */

@@ -57,7 +57,11 @@ def test_packed_weight_bytes_layout(lib):
         assert lib.mxfp4_packed_weight_bytes(N, K) == expect
     assert lib.mxfp4_packed_weight_bytes(16, 48) == 0  # K % 32 != 0
     assert lib.mxfp4_packed_weight_bytes(0, 64) == 0
-    assert lib.mxfp4_workspace_bytes(16, 2112, 7168) == 0
+    assert lib.mxfp4_workspace_bytes(16, 2112, 7168) == 0  # single fused kernel
+    # from M = 64 on: room for the codes and scales of A, each rounded to 256 bytes
+    assert lib.mxfp4_workspace_bytes(64, 7168, 2048) == 64 * 1024 + 64 * 64
+    assert lib.mxfp4_workspace_bytes(100, 128, 96) == 4864 + 512
+    assert lib.mxfp4_workspace_bytes(64, 128, 40) == 0
 
 
 def test_argument_checks_launch_nothing(lib):

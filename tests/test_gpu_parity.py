@@ -122,15 +122,24 @@ def test_gemm_small_full_parity(oracle_mod, M, N, K):
     bq, bs, W = quantized_weight(oracle_mod, B)
     aq, as_, c64, c16 = oracle_mod.quant_gemm(A, bq, bs)
     Ad = A.cuda()
-    C_fused = mx.quant_gemm(Ad, W)
+    C_fused = mx.quant_gemm(Ad, W)  # two-pass route for M >= 64 (workspace from torch)
+    no_ws = torch.empty(0, dtype=torch.uint8, device="cuda")
+    C_single = mx.quant_gemm(Ad, W, workspace=no_ws)  # always the single fused kernel
     Aq, As = mx.quantize(Ad)
     assert np.array_equal(Aq.cpu().numpy(), aq) and np.array_equal(As.cpu().numpy(), as_)
     C_unfused = mx.gemm(Aq, As, W)
     torch.cuda.synchronize()
-    check_close(C_fused, c64, f"fused {M}x{N}x{K}")
+    check_close(C_fused, c64, f"quant_gemm {M}x{N}x{K}")
+    check_close(C_single, c64, f"fused kernel {M}x{N}x{K}")
     check_close(C_unfused, c64, f"unfused {M}x{N}x{K}")
-    # the fused kernel quantizes exactly like the standalone quantizer: same sums
-    assert torch.equal(C_fused, C_unfused)
+    if mx.gemm_plan(M, N, K, fused=True)["two_pass"]:
+        # the two-pass route is mxfp4_quantize + the unfused GEMM: identical sums
+        assert torch.equal(C_fused, C_unfused)
+    p_f, p_u = mx.gemm_plan(M, N, K, fused=True), mx.gemm_plan(M, N, K, fused=False)
+    same = all(p_f[k] == p_u[k] for k in ("block_m", "splits"))
+    if not p_f["two_pass"] and same:
+        # the fused kernel quantizes exactly like the standalone quantizer: same sums
+        assert torch.equal(C_fused, C_unfused)
 
 
 def test_gemm_every_plan_agrees(oracle_mod):
@@ -194,14 +203,18 @@ def test_gemm_full_size_sampled(oracle_mod, name):
     aq, as_ = oracle_mod.quantize(A)
     Ad = A.cuda()
     C = mx.quant_gemm(Ad, W).cpu()
+    C_single = mx.quant_gemm(Ad, W, workspace=torch.empty(0, dtype=torch.uint8, device="cuda")).cpu()
     Aq, As = mx.quantize(Ad)
     C_unfused = mx.gemm(Aq, As, W).cpu()
-    assert torch.equal(C, C_unfused)
     rng = np.random.default_rng(w.seed)
     ms = np.concatenate([rng.integers(0, w.M, 3000), np.full(64, w.M - 1), np.zeros(64, np.int64)])
     ns = np.concatenate([rng.integers(0, w.N, 3000), w.N - 1 - np.arange(64), np.arange(64)])
     c64, _ = oracle_mod.gemm_sampled(aq, as_, bq, bs, ms, ns)
     check_close(C[ms, ns], c64, f"{name} sampled")
+    check_close(C_single[ms, ns], c64, f"{name} sampled, fused kernel")
+    check_close(C_unfused[ms, ns], c64, f"{name} sampled, unfused")
+    if mx.gemm_plan(w.M, w.N, w.K, fused=True)["two_pass"]:
+        assert torch.equal(C, C_unfused)
 
 
 # ----------------------------------------------------------------------------- bounded waits
