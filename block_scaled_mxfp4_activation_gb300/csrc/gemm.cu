@@ -569,9 +569,37 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // when a split has more K tiles), or every K tile of the split when that
 // still fits.  Ties prefer the larger block_m (fewer re-reads of the weights),
 // then the larger stage count, then fewer splits.
+// Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
+// the search below is not: sweeps of block_m x splits x stages, graph-replayed
+// calls with rotating operands.  `fused` is the GEMM kernel's kind (the large-M
+// shapes run the pre-quantized kernel on the fused entry's two-pass route).
+struct TunedPlan {
+  int64_t M, N, K;
+  bool fused;
+  int block_m, splits, stages;
+};
+constexpr TunedPlan kTunedPlans[] = {
+    {16, 2112, 7168, true, 32, 7, 2},
+    {64, 7168, 2048, false, 64, 4, 2},
+    {256, 3072, 1536, false, 64, 2, 3},
+};
+
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                   mxfp4_plan_t* p) {
   *p = mxfp4_plan_t{};
+  if (prop.multiProcessorCount == 152) {
+    for (const TunedPlan& t : kTunedPlans) {
+      if (t.M != M || t.N != N || t.K != K || t.fused != fused) continue;
+      mxfp4_plan_t q{};
+      q.block_m = t.block_m;
+      q.splits = t.splits;
+      q.stages = t.stages;
+      if (finish_plan(M, N, K, fused, prop, &q)) {
+        *p = q;
+        return;
+      }
+    }
+  }
   const int bm0 = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   const int64_t k_tiles = ceil_div(K, kTileK);
   const int64_t cap = 2 * static_cast<int64_t>(prop.multiProcessorCount);
