@@ -231,6 +231,9 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
 }
 
 }  // namespace
+
+void set_last_error(const char* what) { snprintf(g_last_error, sizeof(g_last_error), "%s", what); }
+
 }  // namespace mxfp4
 
 using namespace mxfp4;

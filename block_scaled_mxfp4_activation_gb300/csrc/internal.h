@@ -92,6 +92,8 @@ cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, co
                         const mxfp4_plan_t& plan, bool fused, bool programmatic, cudaStream_t s);
 
 cudaError_t read_device_error(cudaStream_t s, uint32_t* code, bool reset);
+// Sets the calling thread's message for mxfp4_last_error_string().
+void set_last_error(const char* what);
 // Address of the device error word on the current device (nullptr on failure).
 uint32_t* device_error_word();
 

@@ -141,6 +141,33 @@ mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes,
                                 mxfp4_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * mxfp4_quant_gemm_static_scratch -- the fused layer without any allocation.
+ *
+ * The pages have no counterpart: this exists for callers that cannot allocate
+ * device memory -- a plugin inside a host framework that reserves all device
+ * memory up front and forbids allocation afterwards, or code that must not
+ * call cudaMalloc because it synchronises the device -- and so cannot give
+ * mxfp4_quant_gemm the workspace of its two-pass route.  This call always runs
+ * that route (mxfp4_quantize into scratch, then mxfp4_gemm on the codes) with
+ * the scratch in a 4 MiB device array the library owns: every GPU that loads
+ * the library holds it until the process exits.  The caller passes only the
+ * inputs and the output, as for mxfp4_quant_gemm (A bf16 [M, lda], Bpacked, C
+ * bf16 [M, N]); nothing is allocated.
+ *   - Sizes whose codes and scales (M*K/2 + M*K/32 bytes, each rounded up to
+ *     256) exceed 4 MiB return MXFP4_ERR_UNSUPPORTED_SHAPE, launching nothing;
+ *     mxfp4_last_error_string() then names the limit.
+ *   - The first call on a device resolves the array's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents
+ *     (nothing in it needs clearing: each call overwrites what it reads).
+ *     Calls that can overlap on the GPU -- on streams not ordered with each
+ *     other -- race on it.
+ * For M < 64, mxfp4_quant_gemm with no workspace needs no scratch at all and
+ * is faster. */
+mxfp4_status_t mxfp4_quant_gemm_static_scratch(const void* A, int64_t lda, const void* Bpacked, void* C,
+                                               int64_t M, int64_t N, int64_t K, mxfp4_stream_t stream);
+
 /* The plan the two GEMM entries would use for (M, N, K); fused != 0 for the
  * fused entry.  Host only, launches nothing. */
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan);
