@@ -88,6 +88,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             "mxfp4_diag_wait_timeout": ([S], st),
             "mxfp4_set_programmatic_launch": ([ctypes.c_int], st),
             "mxfp4_last_error_string": ([], ctypes.c_char_p),
+            "mxfp4_quant_gemm_host": ([P, I, P, I, P, P, P, I, I, I, P, Z, S], st),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -232,6 +233,22 @@ def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
     _call("mxfp4_quant_gemm", _ptr(A), A.stride(0), _ptr(W.data), _ptr(out), M, W.N, W.K, ws_ptr, ws_bytes,
           _stream(stream))
     return out
+
+
+def quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, C_dev: torch.Tensor,
+                    C_host: torch.Tensor, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The fused layer on host data in one call: A_host (pinned CPU bf16 [M, K]) -> A_dev ->
+    quantize + GEMM -> C_dev -> C_host (pinned CPU bf16 [M, N]); asynchronous on the stream."""
+    W = _weight(W)
+    for t, dev, what in ((A_host, False, "A_host"), (C_host, False, "C_host"), (A_dev, True, "A_dev"),
+                         (C_dev, True, "C_dev")):
+        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.is_cuda != dev or t.stride(-1) != 1:
+            raise TypeError(f"{what} must be a {'CUDA' if dev else 'CPU'} bf16 tensor with unit column stride")
+    M = A_host.shape[0]
+    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel()) if workspace is not None else (None, 0)
+    _call("mxfp4_quant_gemm_host", _ptr(A_host), A_host.stride(0), _ptr(A_dev), A_dev.stride(0), _ptr(W.data),
+          _ptr(C_dev), _ptr(C_host), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream))
+    return C_host
 
 
 def gemm_plan(M: int, N: int, K: int, fused: bool = True) -> dict:

@@ -316,6 +316,29 @@ mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked,
   return run_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, s);
 }
 
+mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void* A_dev, int64_t lda_dev,
+                                     const void* Bpacked, void* C_dev, void* C_host, int64_t M, int64_t N,
+                                     int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  mxfp4_status_t st = check_mnk(M, N, K);
+  if (st != MXFP4_OK) return st;
+  // every check of mxfp4_quant_gemm first, so that an error launches nothing
+  if (A_host == nullptr || C_host == nullptr || A_dev == nullptr || Bpacked == nullptr || C_dev == nullptr)
+    return MXFP4_ERR_INVALID_ARG;
+  if (lda_host < K || lda_dev < K) return MXFP4_ERR_INVALID_ARG;
+  if (!aligned16(A_dev) || !aligned16(Bpacked) || !aligned16(C_dev) || lda_dev % 8 != 0)
+    return MXFP4_ERR_MISALIGNED;
+  if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (current_device(&st) == nullptr) return st;
+  cudaError_t e = cudaMemcpy2DAsync(A_dev, static_cast<size_t>(lda_dev) * 2, A_host, static_cast<size_t>(lda_host) * 2,
+                                    static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return cuda_failure("activation upload", e);
+  st = mxfp4_quant_gemm(A_dev, lda_dev, Bpacked, C_dev, M, N, K, ws, ws_bytes, stream);
+  if (st != MXFP4_OK) return st;
+  e = cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(M) * static_cast<size_t>(N) * 2, cudaMemcpyDeviceToHost, s);
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("result download", e);
+}
+
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan) {
   if (plan == nullptr) return MXFP4_ERR_INVALID_ARG;
   mxfp4_status_t st = check_mnk(M, N, K);

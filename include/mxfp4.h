@@ -141,6 +141,17 @@ mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes,
                                 mxfp4_stream_t stream);
 
+/* The fused entry for activations and results in host memory: uploads A
+ * (host bf16 [M, lda_host]) into A_dev (device bf16 [M, lda_dev]), runs
+ * mxfp4_quant_gemm on it (C_dev, ws as there) and downloads C_dev into C_host
+ * (host bf16 [M, N]) -- three asynchronous operations on `stream`, issued by
+ * one call.  The caller owns every buffer; host buffers should be pinned
+ * (page-locked) for the copies to be asynchronous.  C_host is complete when
+ * the stream is.  All checks precede the upload: an error launches nothing. */
+mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void* A_dev, int64_t lda_dev,
+                                     const void* Bpacked, void* C_dev, void* C_host, int64_t M, int64_t N,
+                                     int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream);
+
 /* ---------------------------------------------------------------------------
  * mxfp4_quant_gemm_static_scratch -- the fused layer without any allocation.
  *

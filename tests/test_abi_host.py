@@ -84,6 +84,9 @@ def test_argument_checks_launch_nothing(lib):
     assert lib.mxfp4_quant_gemm(fake, 68, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED  # lda % 8
     assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 4, 0, 64, None, 0, None) == INVALID
     assert lib.mxfp4_quant_gemm(fake, 1 << 40, fake, fake, 1 << 31, 128, 1 << 31, None, 0, None) == UNSUPPORTED
+    assert lib.mxfp4_quant_gemm_host(None, 64, fake, 64, fake, fake, fake, 4, 128, 64, None, 0, None) == INVALID
+    assert lib.mxfp4_quant_gemm_host(fake, 64, fake, 68, fake, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED
+    assert lib.mxfp4_quant_gemm_host(fake, 64, odd, 64, fake, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED
     assert lib.mxfp4_gemm_plan(4, 128, 64, 1, None) == INVALID
     assert lib.mxfp4_device_error(None, 0, None) == INVALID
 

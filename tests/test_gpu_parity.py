@@ -217,6 +217,22 @@ def test_gemm_full_size_sampled(oracle_mod, name):
         assert torch.equal(C, C_unfused)
 
 
+def test_quant_gemm_host_buffers(oracle_mod):
+    for M, N, K, lda in ((32, 512, 512, 520), (64, 384, 1024, 1024)):
+        A, B = workloads.make_random(M, N, K, seed=M + K)
+        Ah = torch.zeros((M, lda), dtype=torch.bfloat16)
+        Ah[:, :K] = A
+        Ah = Ah.pin_memory()[:, :K]
+        W = mx.quantize_weights(B.cuda())
+        Ad = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+        Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        Ch = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+        mx.quant_gemm_host(Ah, W, Ad, Cd, Ch)
+        torch.cuda.synchronize()
+        assert torch.equal(Ad.cpu(), A)
+        assert torch.equal(Ch, mx.quant_gemm(A.cuda(), W).cpu())
+
+
 # ----------------------------------------------------------------------------- bounded waits
 def test_bounded_wait_reports_instead_of_hanging():
     assert mx.device_error(reset=True) == 0
