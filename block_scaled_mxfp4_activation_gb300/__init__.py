@@ -46,7 +46,7 @@ class MXFP4Error(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "splits", "stages", "k_tiles_per_split", "grid_x", "grid_y", "grid_z", "threads",
-        "smem_bytes", "tmem_cols", "two_pass")]
+        "smem_bytes", "tmem_cols", "two_pass", "accumulators")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -273,6 +273,7 @@ def gemm_with_plan(A_or_Aq: torch.Tensor, As: torch.Tensor | None, W: PackedWeig
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A_or_Aq.device)
     p = Plan()
     p.block_m, p.splits, p.stages = int(plan["block_m"]), int(plan["splits"]), int(plan.get("stages", 0))
+    p.accumulators = int(plan.get("accumulators", 0))
     _call("mxfp4_gemm_with_plan", _ptr(A_or_Aq), lda, _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K,
           int(fused), ctypes.byref(p), _stream(stream))
     return out

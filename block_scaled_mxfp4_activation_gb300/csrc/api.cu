@@ -189,6 +189,7 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
     plan.block_m = user_plan->block_m;
     plan.splits = user_plan->splits;
     plan.stages = user_plan->stages;
+    plan.accumulators = user_plan->accumulators;
     if (!finish_plan(M, N, K, fused, dev->prop, &plan)) return MXFP4_ERR_INVALID_ARG;
   } else {
     cached_default_plan(M, N, K, fused, dev->prop, &plan);
@@ -223,6 +224,7 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   g.bar_off = GL.bar_off;
   g.stg_blocks = GL.stg_blocks;
   g.a_box_rows = activation_box_rows(M, plan.block_m);
+  g.accumulators = plan.accumulators;
   g.weights_early = g_programmatic.load() >= 2 ? 1 : 0;
   g.err = device_error_word();
   if (g.err == nullptr) return failure("cudaGetSymbolAddress (device error word)");

@@ -95,6 +95,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   const int kt_begin = static_cast<int>(rank) * args.kt_per_split;
   const int kt_end = min(args.k_tiles, kt_begin + args.kt_per_split);
   const int kt_count = max(0, kt_end - kt_begin);
+  // K steps (of 64) in this split's last K tile
+  const int steps_last = kt_count > 0 ? min(4, (args.K - (kt_end - 1) * kTileK + 63) / 64) : 0;
   const uint64_t timeout = args.timeout_ns;
 
   if (threadIdx.x == 0) {
@@ -120,7 +122,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  const uint32_t tmem_sf = tmem_base + BM;  // scale columns follow the accumulator
+  const int nacc = args.accumulators;                 // independent accumulators (1, 2 or 4)
+  const uint32_t tmem_sf = tmem_base + nacc * BM;     // scale columns follow the accumulators
 
   // The next call in the stream may start its own prologue now.  Reads of data
   // an earlier grid may write (the activation) and every global write come
@@ -224,8 +227,11 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
           if (k0 + 64 * j >= args.K) break;
           const uint32_t sid = (j & 1) * 2;
           // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 -> +2)
-          mma_mxf4(tmem_base, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>(sid), sfw_t + 4 * (j >> 1),
-                   sfa_t + 4 * C::kRowChunks * (j >> 1), (i | j) != 0);
+          // K step g = 4i + j accumulates into tile g % nacc: nacc independent
+          // chains the tensor core can overlap (summed in the epilogue)
+          const int g = 4 * i + j, acc = g & (nacc - 1);
+          mma_mxf4(tmem_base + acc * BM, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>(sid), sfw_t + 4 * (j >> 1),
+                   sfa_t + 4 * C::kRowChunks * (j >> 1), g >= nacc);
         }
         if (i + stages < kt_count) tc_commit(empty(s));  // frees the stage when these MMAs finish
       }
@@ -345,7 +351,17 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     for (int c = h; c < chunks; c += 2) {
       uint32_t r[16];
       if (have) {
-        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(qr * 32) << 16) + c * 16, r);
+        const uint32_t taddr = tmem_base + (static_cast<uint32_t>(qr * 32) << 16) + c * 16;
+        tmem_ld_32x32b_x16(taddr, r);
+        // accumulators that received no K step (fewer steps than tiles) are skipped
+        const int used = min(nacc, 4 * (kt_count - 1) + steps_last);
+        for (int a = 1; a < used; ++a) {
+          uint32_t t[16];
+          tmem_ld_32x32b_x16(taddr + a * BM, t);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) + __uint_as_float(t[e]));
+        }
         tmem_ld_wait();
       } else {
 #pragma unroll
@@ -502,7 +518,12 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
   p->grid_z = static_cast<int32_t>(ceil_div(M, p->block_m));
   if (p->grid_y > 65535 || p->grid_z > 65535) return false;
   p->threads = threads_for(p->block_m);
-  const uint32_t tcols = pow2_at_least(p->block_m + p->stages * sf_cols_for(p->block_m));
+  // One accumulator by default: on GB300 spreading a CTA's K steps over 2 or 4
+  // independent tiles measured no faster (the MMA phase is dominated by fixed
+  // start-up cost, not by the dependent chain), and it costs tensor memory.
+  if (p->accumulators == 0) p->accumulators = 1;
+  if (p->accumulators != 1 && p->accumulators != 2 && p->accumulators != 4) return false;
+  const uint32_t tcols = pow2_at_least(p->accumulators * p->block_m + p->stages * sf_cols_for(p->block_m));
   if (tcols > 512) return false;
   p->tmem_cols = static_cast<int32_t>(tcols);
   const GemmLayout L = gemm_layout(p->block_m, p->stages, p->splits, fused, M);

@@ -61,6 +61,7 @@ struct GemmArgs {
   uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off;
   int32_t stg_blocks;       // 32 x 16 partial blocks each CTA may receive from one split
   int32_t a_box_rows;       // rows of one activation TMA box: min(block_m, roundup(M, 8))
+  int32_t accumulators;     // independent fp32 accumulator tiles in tensor memory (1, 2, 4)
 };
 
 // Shared-memory layout of one GEMM CTA (byte offsets from a 1024-aligned base):

@@ -64,6 +64,8 @@ typedef struct {
   int32_t two_pass;   /* mxfp4_gemm_plan, fused entry: 1 if, given mxfp4_workspace_bytes() of
                          workspace, it quantizes A into the workspace and runs the GEMM on
                          codes (this plan then describes that GEMM) */
+  int32_t accumulators; /* independent fp32 accumulator tiles in tensor memory: 1, 2 or 4
+                           (K step g goes to tile g mod accumulators; summed in the epilogue) */
 } mxfp4_plan_t;
 
 /* ---------------------------------------------------------------------------
@@ -183,8 +185,9 @@ mxfp4_status_t mxfp4_quant_gemm_static_scratch(const void* A, int64_t lda, const
  * fused entry.  Host only, launches nothing. */
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan);
 
-/* The GEMM entries with an explicit plan: only block_m, splits and stages are
- * read (the rest is derived); a plan the device cannot run is rejected with
+/* The GEMM entries with an explicit plan: only block_m, splits, stages and
+ * accumulators (0 = the default choice) are read (the rest is derived); a plan
+ * the device cannot run is rejected with
  * MXFP4_ERR_INVALID_ARG.  fused != 0 reads A/lda, else Aq/As. */
 mxfp4_status_t mxfp4_gemm_with_plan(const void* A_or_Aq, int64_t lda, const void* As,
                                     const void* Bpacked, void* C, int64_t M, int64_t N, int64_t K,

@@ -170,6 +170,26 @@ def test_gemm_every_plan_agrees(oracle_mod):
     assert len(ran) >= 80, rejected
 
 
+@pytest.mark.parametrize("accumulators", [1, 2, 4])
+def test_gemm_independent_accumulators(oracle_mod, accumulators):
+    # K steps spread over 1, 2 or 4 accumulator tiles, with a ragged last K tile
+    M, N, K = 40, 384, 2048 - 96
+    A, B = workloads.make_random(M, N, K, seed=7 + accumulators)
+    bq, bs, W = quantized_weight(oracle_mod, B)
+    _, _, c64, _ = oracle_mod.quant_gemm(A, bq, bs)
+    Ad = A.cuda()
+    Aq, As = mx.quantize(Ad)
+    for bm, splits, stages in ((64, 2, 4), (64, 1, 2), (32, 8, 1)):
+        plan = {"block_m": bm, "splits": splits, "stages": stages, "accumulators": accumulators}
+        for fused in (True, False):
+            try:
+                C = mx.gemm_with_plan(Ad if fused else Aq, None if fused else As, W, plan, fused)
+            except mx.MXFP4Error as e:
+                assert e.status == 1  # does not fit (tensor or shared memory)
+                continue
+            check_close(C, c64, f"plan {plan} fused={fused}")
+
+
 def test_gemm_deterministic_and_graph_replay(oracle_mod):
     M, N, K = 16, 2112, 7168
     A, B = workloads.make_random(M, N, K, seed=5, b_std=0.02, outlier_frac=0.01)
