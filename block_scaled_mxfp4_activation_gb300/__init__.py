@@ -22,7 +22,7 @@ from . import build as _build
 
 __all__ = [
     "MXFP4Error", "PackedWeight", "load_library", "library_path", "quantize", "packed_weight_bytes",
-    "pack_weights", "unpack_weights", "quantize_weights", "gemm", "quant_gemm", "gemm_plan",
+    "pack_weights", "pack_weights_shuffled", "unpack_weights", "quantize_weights", "gemm", "quant_gemm", "gemm_plan",
     "gemm_with_plan", "workspace_bytes", "device_error", "set_wait_timeout_ns", "diag_wait_timeout",
     "status_string", "Plan", "set_programmatic_launch",
 ]
@@ -77,6 +77,7 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             "mxfp4_packed_weight_bytes": ([I, I], Z),
             "mxfp4_pack_weights": ([P, P, I, I, P, S], st),
             "mxfp4_unpack_weights": ([P, I, I, P, P, S], st),
+            "mxfp4_pack_weights_shuffled": ([P, P, I, I, P, S], st),
             "mxfp4_workspace_bytes": ([I, I, I], Z),
             "mxfp4_gemm": ([P, P, P, P, I, I, I, P, Z, S], st),
             "mxfp4_quant_gemm": ([P, I, P, P, I, I, I, P, Z, S], st),
@@ -160,6 +161,24 @@ def pack_weights(Bq: torch.Tensor, Bs: torch.Tensor, out: torch.Tensor | None = 
         out = torch.empty(packed_weight_bytes(N, K), dtype=torch.uint8, device=Bq.device)
     _call("mxfp4_pack_weights", _ptr(Bq), _ptr(Bs), N, K, _ptr(out), _stream(stream))
     return out
+
+
+def pack_weights_shuffled(B_shuffle: torch.Tensor, B_scale_sh: torch.Tensor, N: int, K: int,
+                          out: torch.Tensor | None = None, stream=None) -> PackedWeight:
+    """The pages' preshuffled weight (B_shuffle) and e8m0-shuffled scales
+    (B_scale_sh) -> a PackedWeight, without going through the natural layout."""
+    for t, what in ((B_shuffle, "B_shuffle"), (B_scale_sh, "B_scale_sh")):
+        if not isinstance(t, torch.Tensor) or not t.is_cuda or not t.is_contiguous():
+            raise TypeError(f"{what} must be a contiguous CUDA tensor")
+    Bsh = B_shuffle.view(torch.uint8)
+    Ssh = B_scale_sh.view(torch.uint8)
+    gp = -(-(K // 32) // 8) * 8
+    if Bsh.numel() < N * K // 2 or Ssh.numel() < -(-N // 32) * 32 * gp:
+        raise ValueError("B_shuffle / B_scale_sh are smaller than their layouts need")
+    if out is None:
+        out = torch.empty(packed_weight_bytes(N, K), dtype=torch.uint8, device=Bsh.device)
+    _call("mxfp4_pack_weights_shuffled", _ptr(Bsh), _ptr(Ssh), N, K, _ptr(out), _stream(stream))
+    return PackedWeight(out, N, K)
 
 
 def unpack_weights(Bp: torch.Tensor, N: int, K: int, stream=None):

@@ -272,6 +272,19 @@ mxfp4_status_t mxfp4_pack_weights(const void* Bq, const void* Bs, int64_t N, int
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("weight packing launch", e);
 }
 
+mxfp4_status_t mxfp4_pack_weights_shuffled(const void* B_shuffle, const void* B_scale_sh, int64_t N, int64_t K,
+                                           void* Bpacked, mxfp4_stream_t stream) {
+  if (B_shuffle == nullptr || B_scale_sh == nullptr || Bpacked == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (N < 1 || K < 64 || N % 16 != 0 || K % 64 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (N > kMaxDim || K > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(Bpacked)) return MXFP4_ERR_MISALIGNED;
+  mxfp4_status_t st;
+  if (current_device(&st) == nullptr) return st;
+  const cudaError_t e =
+      launch_pack_from_shuffled(B_shuffle, B_scale_sh, N, K, Bpacked, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("shuffled weight packing launch", e);
+}
+
 mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, void* Bq, void* Bs,
                                     mxfp4_stream_t stream) {
   if (Bq == nullptr || Bs == nullptr || Bpacked == nullptr) return MXFP4_ERR_INVALID_ARG;

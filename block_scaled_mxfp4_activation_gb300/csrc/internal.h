@@ -79,6 +79,8 @@ cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, vo
                             bool programmatic, cudaStream_t s);
 cudaError_t launch_pack_weights(const void* Bq, const void* Bs, int64_t N, int64_t K, void* Bp,
                                 cudaStream_t s);
+cudaError_t launch_pack_from_shuffled(const void* Bsh, const void* Ssh, int64_t N, int64_t K, void* Bp,
+                                      cudaStream_t s);
 cudaError_t launch_unpack_weights(const void* Bp, int64_t N, int64_t K, void* Bq, void* Bs,
                                   cudaStream_t s);
 cudaError_t launch_diag_wait(uint64_t timeout_ns, cudaStream_t s);

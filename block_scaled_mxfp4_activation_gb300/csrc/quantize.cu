@@ -114,6 +114,40 @@ __global__ void unpack_kernel(const uint8_t* __restrict__ bp, int64_t N, int64_t
   }
 }
 
+// ----------------------------------------------------------------------------- ingest of the pages' layouts
+// Weight codes in the pages' preshuffled layout (submission 748756,
+// `materialize_linear_weight_layout`): 16-row x 16-byte subtiles, byte (n, kb)
+// of the natural [N, K/2] array at ((n/16 * Kh/32 + kb/32) * 2 + (kb%32)/16)
+// * 256 + (n%16) * 16 + kb%16, Kh = K/2.  Scales in the e8m0 shuffle (the
+// store of submission 755056's standalone quantizer, inverted by
+// `materialize_linear_scale_layout`): scale (n, g) at (n/32) * 32 * Gp +
+// (g/8) * 256 + (g%4) * 64 + (n%16) * 4 + ((g%8)/4) * 2 + (n%32)/16, Gp = K/32
+// rounded up to 8.
+__device__ __forceinline__ int64_t shuffled_code_index(int64_t n, int64_t kb, int64_t kh) {
+  return ((n / 16 * (kh / 32) + kb / 32) * 2 + (kb % 32) / 16) * 256 + (n % 16) * 16 + kb % 16;
+}
+
+__device__ __forceinline__ int64_t shuffled_scale_index(int64_t n, int64_t g, int64_t gp) {
+  return (n / 32) * 32 * gp + (g / 8) * 256 + (g % 4) * 64 + (n % 16) * 4 + ((g % 8) / 4) * 2 + (n % 32) / 16;
+}
+
+__global__ void pack_from_shuffled_kernel(const uint8_t* __restrict__ bsh, const uint8_t* __restrict__ ssh,
+                                          int64_t N, int64_t K, int64_t n_pad, int64_t k_tiles,
+                                          uint8_t* __restrict__ out, size_t sf_offset) {
+  const int64_t kh = K / 2, nblk = K / 32, gp = (nblk + 7) / 8 * 8;
+  const int64_t codes = n_pad * kh, scales = n_pad * k_tiles * 8;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < codes + scales;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    if (i < codes) {
+      const int64_t n = i / kh, kb = i % kh;
+      out[i] = n < N ? bsh[shuffled_code_index(n, kb, kh)] : 0;
+    } else {
+      const int64_t j = i - codes, n = j / (k_tiles * 8), g = j % (k_tiles * 8);
+      out[sf_offset + packed_sf_index(n, g, k_tiles)] = (n < N && g < nblk) ? ssh[shuffled_scale_index(n, g, gp)] : 0;
+    }
+  }
+}
+
 static unsigned grid_for(int64_t work, int threads) {
   int64_t b = ceil_div(work, threads);
   if (b > 65536) b = 65536;
@@ -136,6 +170,21 @@ cudaError_t launch_pack_weights(const void* Bq, const void* Bs, int64_t N, int64
   }
   pack_scales_kernel<<<grid_for(L.n_pad * L.k_tiles * 8, 256), 256, 0, s>>>(
       static_cast<const uint8_t*>(Bs), N, L.n_pad, K / 32, L.k_tiles, out + L.sf_offset);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pack_from_shuffled(const void* Bsh, const void* Ssh, int64_t N, int64_t K, void* Bp,
+                                      cudaStream_t s) {
+  const PackedLayout L = packed_layout(N, K);
+  uint8_t* out = static_cast<uint8_t*>(Bp);
+  if (L.sf_offset > L.data_bytes) {
+    const cudaError_t e = cudaMemsetAsync(out + L.data_bytes, 0, L.sf_offset - L.data_bytes, s);
+    if (e != cudaSuccess) return e;
+  }
+  const int64_t work = L.n_pad * (K / 2) + L.n_pad * L.k_tiles * 8;
+  pack_from_shuffled_kernel<<<grid_for(work, 256), 256, 0, s>>>(static_cast<const uint8_t*>(Bsh),
+                                                               static_cast<const uint8_t*>(Ssh), N, K, L.n_pad,
+                                                               L.k_tiles, out, L.sf_offset);
   return cudaGetLastError();
 }
 

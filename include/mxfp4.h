@@ -103,6 +103,23 @@ size_t mxfp4_packed_weight_bytes(int64_t N, int64_t K);
 mxfp4_status_t mxfp4_pack_weights(const void* Bq, const void* Bs, int64_t N, int64_t K, void* Bpacked,
                                   mxfp4_stream_t stream);
 
+/* The same packed buffer from the weight layouts the pages' harness hands out
+ * (`custom_kernel((A, B, B_q, B_shuffle, B_scale_sh))`), so that tuple runs as
+ * it is:
+ *   B_shuffle   device, uint8 [N, K/2] bytes in the preshuffled layout of
+ *               `materialize_linear_weight_layout` (submission 748756):
+ *               16-row x 16-byte subtiles; natural byte (n, kb) at
+ *               ((n/16 * Kh/32 + kb/32) * 2 + (kb%32)/16) * 256 + (n%16) * 16 + kb%16,
+ *               Kh = K/2.
+ *   B_scale_sh  device, uint8, the e8m0 shuffle (`materialize_linear_scale_layout`;
+ *               the shuffled-scale store of submission 755056): scale (n, g) at
+ *               (n/32) * 32 * Gp + (g/8) * 256 + (g%4) * 64 + (n%16) * 4
+ *               + ((g%8)/4) * 2 + (n%32)/16, Gp = K/32 rounded up to 8; at least
+ *               roundup(N, 32) * Gp bytes (aiter pads the rows to 256).
+ * N % 16 == 0 and K % 64 == 0 (the layouts' own granularity). */
+mxfp4_status_t mxfp4_pack_weights_shuffled(const void* B_shuffle, const void* B_scale_sh, int64_t N, int64_t K,
+                                           void* Bpacked, mxfp4_stream_t stream);
+
 /* Inverse of mxfp4_pack_weights (for checking a packed buffer). */
 mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, void* Bq, void* Bs,
                                     mxfp4_stream_t stream);

@@ -87,6 +87,9 @@ def test_argument_checks_launch_nothing(lib):
     assert lib.mxfp4_quant_gemm_host(None, 64, fake, 64, fake, fake, fake, 4, 128, 64, None, 0, None) == INVALID
     assert lib.mxfp4_quant_gemm_host(fake, 64, fake, 68, fake, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED
     assert lib.mxfp4_quant_gemm_host(fake, 64, odd, 64, fake, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED
+    assert lib.mxfp4_pack_weights_shuffled(fake, fake, 24, 128, fake, None) == INVALID  # N % 16
+    assert lib.mxfp4_pack_weights_shuffled(fake, fake, 32, 96, fake, None) == INVALID  # K % 64
+    assert lib.mxfp4_pack_weights_shuffled(fake, fake, 32, 128, odd, None) == MISALIGNED
     assert lib.mxfp4_gemm_plan(4, 128, 64, 1, None) == INVALID
     assert lib.mxfp4_device_error(None, 0, None) == INVALID
 
