@@ -173,6 +173,20 @@ class Problem:
         return g
 
 
+def aggregate_over_ranks(ms_local: float, steps: int, world: int) -> tuple[float, float]:
+    """The job's time is the slowest rank's (all_reduce MAX over the process
+    group when world > 1); the whole-job value is that time per call over all
+    ranks' calls (every rank runs `steps` independent calls: replicas, weak
+    scaling).  Returns (max ms, us per call for the whole job)."""
+    times = torch.tensor([ms_local], dtype=torch.float64)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.all_reduce(times, op=dist.ReduceOp.MAX)
+    ms_max = float(times[0])
+    return ms_max, ms_max * 1e3 / (steps * world)
+
+
 def time_graph_steps(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, rotate: bool = True,
                      barrier=None):
     """Exactly `steps` calls (graph replays), after `warmup` calls; returns ms."""
@@ -295,14 +309,8 @@ def run_ours(args) -> dict:
     with ClockSampler(local) as clk:
         ms = time_graph_steps(prob, args.steps, warmup, stream, barrier=barrier)
     clocks = clk.summary()
-    times = torch.tensor([ms], dtype=torch.float64)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.all_reduce(times, op=dist.ReduceOp.MAX)
-    ms_total = float(times[0])
+    ms_total, value = aggregate_over_ranks(ms, args.steps, world)
     us_call = ms_total * 1e3 / args.steps
-    value = us_call / world  # whole-job: world * steps calls in the max-over-ranks time
 
     ms_warm = time_graph_steps(prob, min(args.steps, 2000), warmup, stream, rotate=False)
     us_warm = ms_warm * 1e3 / min(args.steps, 2000)

@@ -24,7 +24,7 @@ __all__ = [
     "MXFP4Error", "PackedWeight", "load_library", "library_path", "quantize", "packed_weight_bytes",
     "pack_weights", "pack_weights_shuffled", "unpack_weights", "quantize_weights", "gemm", "quant_gemm", "gemm_plan",
     "gemm_with_plan", "workspace_bytes", "device_error", "set_wait_timeout_ns", "diag_wait_timeout",
-    "status_string", "Plan", "set_programmatic_launch",
+    "status_string", "Plan", "set_programmatic_launch", "custom_kernel", "quant_gemm_host",
 ]
 
 MXFP4_OK = 0
@@ -321,3 +321,27 @@ def set_programmatic_launch(mode: int) -> None:
 
 def diag_wait_timeout(stream=None) -> None:
     _call("mxfp4_diag_wait_timeout", _stream(stream))
+
+
+# ----------------------------------------------------------------------------- the pages' interface
+_packed_cache: dict = {}
+
+
+def custom_kernel(data) -> torch.Tensor:
+    """The leaderboard's interface: data = (A, B, B_q, B_shuffle, B_scale_sh) with A bf16 [M, K],
+    B_shuffle the preshuffled codes and B_scale_sh the e8m0-shuffled scales of the weight
+    (B and B_q are not needed); returns bf16 C [M, N] = A quantized to MXFP4 times the weight.
+
+    The packed weight is built once per (buffers, version) and reused, as the pages cache
+    their weight relayouts."""
+    A, B, _B_q, B_shuffle, B_scale_sh = data
+    N, K = B.shape[0], A.shape[1]
+    key = (B_shuffle.data_ptr(), B_scale_sh.data_ptr(), N, K, B_shuffle._version, B_scale_sh._version)
+    W = _packed_cache.get(key)
+    if W is None:
+        if len(_packed_cache) > 64:
+            _packed_cache.clear()
+        W = pack_weights_shuffled(B_shuffle.contiguous(), B_scale_sh.contiguous(), N, K)
+        _packed_cache[key] = W
+    return quant_gemm(A, W)
+

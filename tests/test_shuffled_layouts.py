@@ -54,3 +54,25 @@ def test_pack_from_shuffled_equals_pack_from_natural(N, K):
     assert torch.equal(W.data, natural)
     q2, s2 = mx.unpack_weights(W.data, N, K)
     assert np.array_equal(q2.cpu().numpy(), q) and np.array_equal(s2.cpu().numpy(), s)
+
+
+@pytest.mark.gpu
+def test_custom_kernel_runs_the_pages_tuple(oracle_mod):
+    """The harness tuple (A, B, B_q, B_shuffle, B_scale_sh), B quantized with the
+    pages' rule (the oracle), through the pages' entry point name."""
+    import block_scaled_mxfp4_activation_gb300 as mx
+    import workloads
+
+    M, N, K = 32, 2880, 512
+    A, B = workloads.make_random(M, N, K, seed=12)
+    bq, bs = oracle_mod.quantize(B)
+    data = (A.cuda(), B.cuda(), torch.from_numpy(bq).cuda(), torch.from_numpy(shuffle_codes(bq)).cuda(),
+            torch.from_numpy(shuffle_scales(bs)).cuda())
+    C = mx.custom_kernel(data)
+    C2 = mx.custom_kernel(data)  # the cached packed weight
+    _, _, c64, _ = oracle_mod.quant_gemm(A, bq, bs)
+    got = C.float().cpu().numpy().astype(np.float64)
+    rms = float(np.sqrt(np.mean(c64 ** 2)))
+    assert np.all(np.abs(got - c64) <= 8e-3 * np.abs(c64) + 1e-2 * rms)
+    assert torch.equal(C, C2)
+
