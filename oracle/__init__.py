@@ -22,12 +22,21 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "mxfp4_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build")
 _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+# Tests that plant a mistake in a copy of the oracle point this variable at
+# the copy's compiled library; nothing else sets it.
+_VARIANT = os.environ.get("MXFP4_ORACLE_VARIANT_LIB")
 _lock = threading.Lock()
 _lib = None
 
 # Plain ISO C, no fast-math and no FMA contraction: the oracle's arithmetic is
 # exactly what the source says.
 _CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def compile_source(src: str, out: str) -> str:
+    """Compile an oracle source file into a shared library with the oracle's flags."""
+    subprocess.run(["gcc", *_CFLAGS, src, "-o", out, "-lm"], check=True)
+    return out
 
 
 def build(force: bool = False) -> str:
@@ -45,7 +54,7 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(build())
+            lib = ctypes.CDLL(_VARIANT if _VARIANT else build())
             P = ctypes.c_void_p
             I = ctypes.c_int64
             lib.oracle_e2m1_decode.argtypes = [ctypes.c_uint8]
