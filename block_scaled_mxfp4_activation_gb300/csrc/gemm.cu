@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
         report_error(args.err, kErrWaitTma);
         *abort_flag = 1u;
       }
-      if (*abort_flag) break;
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;  // warp-uniform: the shuffles below need every lane
       uint8_t* a_tile = smem + args.a_off + s * C::kATileBytes;
       uint8_t* sfa = smem + args.sfa_off + s * C::kSfaStageBytes;
       if constexpr (kFused) {
@@ -367,11 +367,23 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) r[e] = 0u;
       }
+      if (splits == 1) {
+        // no K split: bf16 straight from the accumulator registers to C
+        // (lane = weight row n, register e = activation row m)
+        const int n = n_tile * kTileN + qr * 32 + lane;
+        if (n < args.N) {
+          __nv_bfloat16* col = args.c + static_cast<int64_t>(m_base) * args.N + n;
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            if (c * 16 + e < m_valid) col[static_cast<int64_t>(c * 16 + e) * args.N] = __float2bfloat16_rn(__uint_as_float(r[e]));
+        }
+        continue;
+      }
       const int bi = 4 * c + qr;
       const uint32_t owner = static_cast<uint32_t>(bi % splits);
       const uint32_t dst = sbase + args.stg_off +
                            (static_cast<uint32_t>(rank) * args.stg_blocks + bi / splits) * kBlockBytes + lane * 4;
-      if (splits == 1) {
+      if (owner == rank) {  // this CTA's own blocks: plain shared-memory stores
 #pragma unroll
         for (int e = 0; e < 16; ++e)
           *reinterpret_cast<float*>(smem + (dst - sbase) + e * 128) = __uint_as_float(r[e]);
@@ -390,7 +402,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, args.tmem_cols);
   }
-  if (warp >= 2) {
+  if (warp >= 2 && splits > 1) {
     // ------------------------------------------------ sum the owned blocks over the splits, store bf16
     // Only local shared memory is read from here on, so no CTA waits for its
     // peers before exiting.
@@ -399,16 +411,16 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     const int mine = (valid_blocks - static_cast<int>(rank) + splits - 1) / splits;
     const int n_base = n_tile * kTileN;
     const bool vec_ok = (args.N % 4) == 0;
-    const uint8_t* stg = smem + args.stg_off;
+    const uint32_t stg = sbase + args.stg_off;  // shared-window address: ld.shared, not generic loads
     for (int it = tid; it < mine * 128; it += C::kAThreads) {
       const int lb = it >> 7, w = it & 127, row = w >> 3, c4 = w & 7;
       const int bi = lb * splits + static_cast<int>(rank);
       const int m = (bi >> 2) * 16 + row;
       if (m >= m_valid) continue;
       const uint32_t off = lb * kBlockBytes + row * 128 + c4 * 16;
-      float4 acc = *reinterpret_cast<const float4*>(stg + off);
+      float4 acc = ld_shared_f4(stg + off);
       for (int src = 1; src < splits; ++src) {
-        const float4 p = *reinterpret_cast<const float4*>(stg + src * args.stg_blocks * kBlockBytes + off);
+        const float4 p = ld_shared_f4(stg + src * args.stg_blocks * kBlockBytes + off);
         acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
       }
       const int64_t gm = static_cast<int64_t>(m_base) + m;
@@ -497,7 +509,7 @@ GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t 
   L.stg_off = L.sfa_off + st * (bm > 128 ? 2u : 1u) * 2u * kSfChunkBytes;
   const int64_t rows = M < block_m ? M : block_m;
   const int blocks = static_cast<int>(4 * ceil_div(rows, 16));
-  L.stg_blocks = static_cast<int32_t>(ceil_div(blocks, splits));
+  L.stg_blocks = splits > 1 ? static_cast<int32_t>(ceil_div(blocks, splits)) : 0;  // no split: direct stores
   L.bar_off = L.stg_off + static_cast<uint32_t>(splits * L.stg_blocks) * kBlockBytes;
   L.total = L.bar_off + (4 * st + 1) * 8 + 16;
   return L;
