@@ -103,7 +103,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_w(s), 1);
       mbar_init(full_in(s), 1);
-      mbar_init(full_a(s), C::kAThreads);
+      mbar_init(full_a(s), C::kAWarps);  // one arrival per producer warp
       mbar_init(empty(s), 1);
     }
     mbar_init(accum_bar, 1);
@@ -133,95 +133,115 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      const uint64_t policy_b = policy_evict_first();  // weights: read once per call
-      const uint64_t policy_a = policy_evict_last();   // activations: shared by every N tile
-      const int pre = min(stages, kt_count);
-      auto issue_w = [&](int i) {
-        const int s = i % stages, kt = kt_begin + i;
-        mbar_arrive_expect_tx(full_w(s), C::kBTileBytes + kSfTileBytes);
-        tma_load_2d(sbase + s * C::kBTileBytes, &tmap_b, kt * kTileKBytes, n_tile * kTileN, full_w(s), policy_b);
-        bulk_load(sbase + args.sfw_off + s * kSfTileBytes,
-                  args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes, kSfTileBytes,
-                  full_w(s), policy_b);
-      };
-      auto issue_a = [&](int i) {
-        const int s = i % stages, kt = kt_begin + i;
-        if constexpr (kFused) {
-          mbar_arrive_expect_tx(full_in(s), args.a_box_rows * kTileK * 2);
-          tma_load_2d(sbase + args.abf_off + s * C::kAbfBytes, &tmap_a, kt * kTileK, m_base, full_in(s), policy_a);
-        } else {
-          mbar_arrive_expect_tx(full_in(s), args.a_box_rows * kTileKBytes);
-          tma_load_2d(sbase + args.a_off + s * C::kATileBytes, &tmap_a, kt * kTileKBytes, m_base, full_in(s),
-                      policy_a);
+    // The whole warp runs the loop, so waits, addresses and coordinates stay
+    // warp-uniform; one elected lane issues the copies.
+    const bool leader = elect_one();
+    const uint64_t policy_b = policy_evict_first();  // weights: read once per call
+    const uint64_t policy_a = policy_evict_last();   // activations: shared by every N tile
+    const int pre = min(stages, kt_count);
+    auto issue_w = [&](int i) {
+      const int s = i % stages, kt = kt_begin + i;
+      const uint32_t bar = full_w(s), dst_b = sbase + s * C::kBTileBytes, dst_sf = sbase + args.sfw_off + s * kSfTileBytes;
+      const uint8_t* src_sf = args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes;
+      if (leader) {
+        mbar_arrive_expect_tx(bar, C::kBTileBytes + kSfTileBytes);
+        tma_load_2d(dst_b, &tmap_b, kt * kTileKBytes, n_tile * kTileN, bar, policy_b);
+        bulk_load(dst_sf, src_sf, kSfTileBytes, bar, policy_b);
+      }
+    };
+    auto issue_a = [&](int i) {
+      const int s = i % stages, kt = kt_begin + i;
+      const uint32_t bar = full_in(s);
+      if constexpr (kFused) {
+        const uint32_t dst = sbase + args.abf_off + s * C::kAbfBytes;
+        if (leader) {
+          mbar_arrive_expect_tx(bar, args.a_box_rows * kTileK * 2);
+          tma_load_2d(dst, &tmap_a, kt * kTileK, m_base, bar, policy_a);
         }
-      };
-      if (args.weights_early) {
-        for (int i = 0; i < pre; ++i) issue_w(i);
       } else {
-        for (int i = 0; i < kt_count; ++i) {
-          const int kt = kt_begin + i;
+        const uint32_t dst = sbase + args.a_off + s * C::kATileBytes;
+        if (leader) {
+          mbar_arrive_expect_tx(bar, args.a_box_rows * kTileKBytes);
+          tma_load_2d(dst, &tmap_a, kt * kTileKBytes, m_base, bar, policy_a);
+        }
+      }
+    };
+    if (args.weights_early) {
+      for (int i = 0; i < pre; ++i) issue_w(i);
+    } else {
+      for (int i = 0; i < kt_count; ++i) {
+        const int kt = kt_begin + i;
+        const uint8_t* src_sf = args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes;
+        if (leader) {
           tma_prefetch_l2_2d(&tmap_b, kt * kTileKBytes, n_tile * kTileN);
-          bulk_prefetch_l2(args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes,
-                           kSfTileBytes);
+          bulk_prefetch_l2(src_sf, kSfTileBytes);
         }
       }
-      for (int i = 0; i < kt_count; ++i)
-        tma_prefetch_l2_2d(&tmap_a, kFused ? (kt_begin + i) * kTileK : (kt_begin + i) * kTileKBytes, m_base);
-      grid_dependency_wait();
-      if (!args.weights_early)
-        for (int i = 0; i < pre; ++i) issue_w(i);
-      for (int i = 0; i < pre; ++i) issue_a(i);
-      int issued = pre;
-      for (int i = pre; i < kt_count; ++i) {
-        const int s = i % stages, round = i / stages;
-        if (!mbar_wait(empty(s), (round - 1) & 1, timeout)) {
-          report_error(args.err, kErrWaitEmpty);
-          *abort_flag = 1u;
-        }
-        if (*abort_flag) break;
-        issue_w(i);
-        issue_a(i);
-        issued = i + 1;
+    }
+    for (int i = 0; i < kt_count; ++i) {
+      const int x = kFused ? (kt_begin + i) * kTileK : (kt_begin + i) * kTileKBytes;
+      if (leader) tma_prefetch_l2_2d(&tmap_a, x, m_base);
+    }
+    grid_dependency_wait();
+    if (!args.weights_early)
+      for (int i = 0; i < pre; ++i) issue_w(i);
+    for (int i = 0; i < pre; ++i) issue_a(i);
+    int issued = pre;
+    for (int i = pre; i < kt_count; ++i) {
+      const int s = i % stages, round = i / stages;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty(s), (round - 1) & 1, timeout))) {
+        if (leader) report_error(args.err, kErrWaitEmpty);
+        *abort_flag = 1u;
       }
-      // Before the CTA can exit, every copy it issued must have landed.
-      for (int s = 0; s < stages && s < issued; ++s) {
-        const uint32_t parity = ((s + stages * ((issued - 1 - s) / stages)) / stages) & 1;
-        if (!mbar_wait(full_w(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
-        if (!mbar_wait(full_in(s), parity, timeout)) report_error(args.err, kErrWaitDrain);
-      }
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+      issue_w(i);
+      issue_a(i);
+      issued = i + 1;
+    }
+    // Before the CTA can exit, every copy it issued must have landed.
+    for (int s = 0; s < stages && s < issued; ++s) {
+      const uint32_t parity = ((s + stages * ((issued - 1 - s) / stages)) / stages) & 1;
+      if (!mbar_wait(full_w(s), parity, timeout) && leader) report_error(args.err, kErrWaitDrain);
+      if (!mbar_wait(full_in(s), parity, timeout) && leader) report_error(args.err, kErrWaitDrain);
     }
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      for (int i = 0; i < kt_count; ++i) {
-        const int s = i % stages, round = i / stages;
-        if (!mbar_wait(full_w(s), round & 1, timeout)) {
-          report_error(args.err, kErrWaitTma);
-          *abort_flag = 1u;
-        }
-        if (*abort_flag) break;
-        tc_fence_after_sync();
-        const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
-        const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
-        const uint32_t sfw_s = sbase + args.sfw_off + s * kSfTileBytes;
-        const uint32_t sfa_s = sbase + args.sfa_off + s * C::kSfaStageBytes;
-        // the weight scales can move to tensor memory while the activation is still being prepared
+    // Warp-wide loop (uniform operands), one elected lane issues the tcgen05
+    // instructions; the same lane issues every commit, which tracks that
+    // lane's earlier operations.
+    const bool leader = elect_one();
+    for (int i = 0; i < kt_count; ++i) {
+      const int s = i % stages, round = i / stages;
+      const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
+      const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
+      const uint32_t sfw_s = sbase + args.sfw_off + s * kSfTileBytes;
+      const uint32_t sfa_s = sbase + args.sfa_off + s * C::kSfaStageBytes;
+      const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
+      const uint64_t b_desc = smem_desc(sbase + args.a_off + s * C::kATileBytes, 16, 1024, 2);
+      const int k0 = (kt_begin + i) * kTileK;
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_w(s), round & 1, timeout))) {
+        if (leader) report_error(args.err, kErrWaitTma);
+        *abort_flag = 1u;
+      }
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+      tc_fence_after_sync();
+      // the weight scales can move to tensor memory while the activation is still being prepared
+      if (leader) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) tmem_cp_32x128b_warpx4(sfw_t + 4 * c, smem_desc(sfw_s + c * kSfChunkBytes, 128, 128, 0));
-        if (!mbar_wait(full_a(s), round & 1, timeout)) {
-          report_error(args.err, kErrWaitA);
-          *abort_flag = 1u;
-        }
-        if (*abort_flag) break;
-        tc_fence_after_sync();
+      }
+      __syncwarp();
+      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_a(s), round & 1, timeout))) {
+        if (leader) report_error(args.err, kErrWaitA);
+        *abort_flag = 1u;
+      }
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+      tc_fence_after_sync();
+      if (leader) {
 #pragma unroll
         for (int c = 0; c < 2 * C::kRowChunks; ++c)
           tmem_cp_32x128b_warpx4(sfa_t + 4 * c, smem_desc(sfa_s + c * kSfChunkBytes, 128, 128, 0));
-        const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
-        const uint64_t b_desc = smem_desc(sbase + args.a_off + s * C::kATileBytes, 16, 1024, 2);
-        const int k0 = (kt_begin + i) * kTileK;
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           if (k0 + 64 * j >= args.K) break;
@@ -235,19 +255,24 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
         }
         if (i + stages < kt_count) tc_commit(empty(s));  // frees the stage when these MMAs finish
       }
-      tc_commit(accum_bar);  // always: the epilogue waits on it
+      __syncwarp();
     }
+    if (leader) tc_commit(accum_bar);  // always: the epilogue waits on it
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ activation producer
     const int tid = threadIdx.x - 64;
     grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
-    constexpr int kUnits = BM * 32 / C::kAThreads;     // fused: 16-byte bf16 units per thread and K tile
-    constexpr int kRowsPerPass = C::kAThreads / 32;   // unit t of a warp covers row warp_row + t * kRowsPerPass
-    constexpr int kBatch = kUnits < 4 ? kUnits : 4;
-    const int warp_row = tid >> 5;
-    const int t_end = m_valid > warp_row ? min(kUnits, (m_valid - warp_row + kRowsPerPass - 1) / kRowsPerPass) : 0;
-    const int b = lane >> 2, q = lane & 3;
+    // fused: units of 16 bf16 (32 bytes), two per 32-element block; unit
+    // u = tid + kAThreads * k is row u / 16, block (u / 2) % 8, half u % 2, so
+    // warp w covers rows 2w + 16k and 2w + 16k + 1
+    constexpr int kUnits = BM * 16 / C::kAThreads;
+    // (batches of up to 4 units below block_m 128, 2 above: registers stay under
+    // 102 per thread, so two CTAs fit on an SM)
+    constexpr int kBatch = kUnits < (BM < 128 ? 4 : 2) ? kUnits : (BM < 128 ? 4 : 2);
+    const int pw = tid >> 5;
+    const int rot = (lane >> 2) & 1;  // which half of its 32 bytes a lane loads first: no bank conflicts
+    const int half = lane & 1;        // which 16 elements of the block the lane owns
     const int64_t nblk = args.K / 32;
     // unfused: the 8 scale bytes of row `tid` for K tile i (one row per thread;
     // block_m <= 256 = the producer thread count)
@@ -284,26 +309,36 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
       uint8_t* a_tile = smem + args.a_off + s * C::kATileBytes;
       uint8_t* sfa = smem + args.sfa_off + s * C::kSfaStageBytes;
       if constexpr (kFused) {
-        // Quantize the staged bf16 tile: 16-byte units, 32 per row (256 bf16);
-        // the 4 lanes of a quad share a 32-element block; rows past M are
-        // skipped (their output columns are never stored).
+        // Quantize the staged bf16 tile (256 bf16 = 512 bytes per row): each
+        // lane pair shares a block's maximum through one shuffle; a warp
+        // skips a unit whose two rows are both past M (their output columns
+        // are never stored).
         const uint8_t* abf = smem + args.abf_off + s * C::kAbfBytes;
-        for (int t0 = 0; t0 < t_end; t0 += kBatch) {
-          uint4 v[kBatch];  // all loads of a batch first, then the independent chains
+#pragma unroll(BM < 256 ? kUnits : 1)
+        for (int k0 = 0; k0 < kUnits; k0 += kBatch) {
+          uint4 v[kBatch][2];  // all loads of a batch first, then the independent chains
 #pragma unroll
           for (int e = 0; e < kBatch; ++e) {
-            const int m = warp_row + (t0 + e) * kRowsPerPass;
-            v[e] = (t0 + e < t_end) ? *reinterpret_cast<const uint4*>(abf + m * (kTileK * 2) + lane * 16)
-                                    : make_uint4(0, 0, 0, 0);
+            const uint8_t* src = abf + (tid + (k0 + e) * C::kAThreads) * 32;
+            if (2 * pw + 16 * (k0 + e) < m_valid) {
+              v[e][0] = *reinterpret_cast<const uint4*>(src + 16 * rot);  // 16 bytes rot, then 16 bytes rot ^ 1
+              v[e][1] = *reinterpret_cast<const uint4*>(src + 16 * (rot ^ 1));
+            }
           }
 #pragma unroll
           for (int e = 0; e < kBatch; ++e) {
-            const int m = warp_row + (t0 + e) * kRowsPerPass;
-            uint32_t byte;
-            const uint32_t codes = quantize_quad(v[e], &byte);
-            if (t0 + e < t_end) {
-              *reinterpret_cast<uint32_t*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + q * 4) = codes;
-              if (q == 0)
+            if (2 * pw + 16 * (k0 + e) >= m_valid) continue;  // warp-uniform
+            const int u = tid + (k0 + e) * C::kAThreads;
+            const int m = u >> 4, b = (u >> 1) & 7;
+            uint32_t amax = absmax16_bf16(v[e][0], v[e][1]);
+            amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            const uint32_t byte = scale_byte_from_amax(amax);
+            const uint16_t sbf = scale_bf16_from_byte(byte);
+            const uint32_t c0 = e2m1_pack8(v[e][0], sbf), c1 = e2m1_pack8(v[e][1], sbf);
+            const uint32_t w0 = rot ? c1 : c0, w1 = rot ? c0 : c1;  // back to memory order
+            if (m < m_valid) {
+              *reinterpret_cast<uint2*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + 8 * half) = make_uint2(w0, w1);
+              if (half == 0)
                 sfa[((b >> 2) * C::kRowChunks + (m >> 7)) * kSfChunkBytes + sf_chunk_offset(m) + (b & 3)] =
                     static_cast<uint8_t>(byte);
             }
@@ -331,8 +366,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
           *reinterpret_cast<uint32_t*>(sfa + (1 * C::kRowChunks + (r >> 7)) * kSfChunkBytes + sf_chunk_offset(r)) = w1;
         }
       }
-      fence_proxy_async_smem();  // make the generic stores visible to tcgen05
-      mbar_arrive(full_a(s));
+      fence_proxy_async_smem();  // make this thread's generic stores visible to tcgen05
+      __syncwarp();              // ... and ordered before the warp's single arrival
+      if (lane == 0) mbar_arrive(full_a(s));
     }
 
     // ------------------------------------------------------------------ epilogue: push partial blocks

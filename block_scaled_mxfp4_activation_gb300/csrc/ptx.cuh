@@ -48,6 +48,17 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
+// One lane of the (fully converged) warp gets true: the lowest-numbered lane.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(bar),
                "r"(bytes)
@@ -271,19 +282,6 @@ __device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
                : "r"(caddr)
                : "memory");
   return v;
-}
-
-// ----------------------------------------------------------------------------- E2M1
-// Two fp32 values -> one byte of E2M1 codes, round to nearest even, saturating
-// at +-6: `hi` lands in bits 7..4, `lo` in bits 3..0.
-__device__ __forceinline__ uint32_t cvt_e2m1x2(float hi, float lo) {
-  uint16_t r;
-  asm("{\n\t.reg .b8 t;\n\t"
-      "cvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\t"
-      "cvt.u16.u8 %0, t;\n\t}"
-      : "=h"(r)
-      : "f"(hi), "f"(lo));
-  return r;
 }
 
 }  // namespace mxfp4

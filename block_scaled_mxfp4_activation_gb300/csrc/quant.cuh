@@ -1,7 +1,7 @@
 // MXFP4 block quantization arithmetic shared by the standalone quantize kernel
-// and the fused GEMM's activation producer.  One thread owns 8 consecutive
-// bf16 values (16 bytes); four adjacent lanes own one 32-element block and
-// combine their maxima with two butterfly shuffles.
+// (four adjacent lanes own one 32-element block, 8 bf16 values each, and
+// combine their maxima with two butterfly shuffles) and the fused GEMM's
+// activation producer (two lanes per block, 16 values each, one shuffle).
 //
 // Rule (amd-mxfp4-mm submission 748756, `hw_pack_mxfp4`; submission 755056,
 // "Software MXFP4 quant"): amax = max |x| over the block; u = (bits(amax) +
@@ -35,25 +35,54 @@ __device__ __forceinline__ uint32_t scale_byte_from_amax(uint32_t amax_bf16) {
   return static_cast<uint32_t>(s + 127);
 }
 
-// 2^-s for scale byte s + 127; a normal fp32 for every byte a finite input
-// produces (0..253).
-__device__ __forceinline__ float inv_scale_from_byte(uint32_t byte) {
-  return __uint_as_float((254u - byte) << 23);
+// Largest |x| of 16 bf16 values (two 16-byte words), as a bf16 bit pattern.
+__device__ __forceinline__ uint32_t absmax16_bf16(uint4 v, uint4 w) {
+  const uint32_t m = 0x7FFF7FFFu;
+  uint32_t a = __vmaxu2(v.x & m, v.y & m);
+  uint32_t b = __vmaxu2(v.z & m, v.w & m);
+  a = __vmaxu2(a, __vmaxu2(w.x & m, w.y & m));
+  b = __vmaxu2(b, __vmaxu2(w.z & m, w.w & m));
+  a = __vmaxu2(a, b);
+  return max(a & 0xFFFFu, a >> 16);
+}
+
+// 2^-s for scale byte s + 127, as a bf16 bit pattern: a normal number for
+// every byte a finite input produces (0..253).
+__device__ __forceinline__ uint16_t scale_bf16_from_byte(uint32_t byte) {
+  return static_cast<uint16_t>((254u - byte) << 7);
 }
 
 // 8 bf16 values (one 16-byte word, element i in half i of the vector) times
 // 2^-s -> 8 E2M1 codes in 4 bytes, element 2i in the low nibble of byte i.
-// x * 2^-s is exact in fp32 whenever it matters (its magnitude is at least
-// 2^-126 or the code is 0 either way), and __fmul_rn keeps subnormal inputs.
-__device__ __forceinline__ uint32_t e2m1_pack8(uint4 v, float inv) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-  uint32_t out = 0;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __fmul_rn(__uint_as_float(w[i] << 16), inv);
-    const float hi = __fmul_rn(__uint_as_float(w[i] & 0xFFFF0000u), inv);
-    out |= cvt_e2m1x2(hi, lo) << (8 * i);
-  }
+// The product is formed by mixed-precision FMAs straight from the bf16 halves
+// (bf16 x bf16 + fp32 -> fp32): x * 2^-s is exact in fp32 whenever it matters
+// (its magnitude is at least 2^-126 or the code is 0 either way), and the
+// addend -0 leaves every product unchanged, including the sign of a zero.
+// The four code bytes are gathered into one 32-bit word directly.
+__device__ __forceinline__ uint32_t e2m1_pack8(uint4 v, uint16_t scale_bf16) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 l0, h0, l1, h1, l2, h2, l3, h3;\n\t"
+      ".reg .f32 y0, y1, y2, y3, y4, y5, y6, y7;\n\t"
+      ".reg .b8 c0, c1, c2, c3;\n\t"
+      "mov.b32 {l0, h0}, %1;\n\t"
+      "mov.b32 {l1, h1}, %2;\n\t"
+      "mov.b32 {l2, h2}, %3;\n\t"
+      "mov.b32 {l3, h3}, %4;\n\t"
+      "fma.rn.f32.bf16 y0, l0, %5, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y1, h0, %5, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y2, l1, %5, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y3, h1, %5, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y4, l2, %5, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y5, h2, %5, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y6, l3, %5, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y7, h3, %5, 0f80000000;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, y1, y0;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c1, y3, y2;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c2, y5, y4;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c3, y7, y6;\n\t"
+      "mov.b32 %0, {c0, c1, c2, c3};\n\t}"
+      : "=r"(out)
+      : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "h"(scale_bf16));
   return out;
 }
 
@@ -66,7 +95,7 @@ __device__ __forceinline__ uint32_t quantize_quad(uint4 v, uint32_t* byte_out) {
   amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
   const uint32_t byte = scale_byte_from_amax(amax);
   *byte_out = byte;
-  return e2m1_pack8(v, inv_scale_from_byte(byte));
+  return e2m1_pack8(v, scale_bf16_from_byte(byte));
 }
 
 }  // namespace mxfp4

@@ -142,6 +142,62 @@ def test_gemm_small_full_parity(oracle_mod, M, N, K):
         assert torch.equal(C_fused, C_unfused)
 
 
+def grid_activation(M: int, K: int, seed: int) -> torch.Tensor:
+    """A bf16 activation made to land on E2M1's rounding ties.  Most 32-element
+    blocks hold multiples of 2^e / 4 between -6 * 2^e and 6 * 2^e, with one
+    element at +-6 * 2^e (e random per block), so every halfway point of the
+    E2M1 grid (0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5 times 2^e) occurs; some
+    elements are -0.0 or tiny (2^(e-12)); some blocks are plain normal values,
+    some all zero.  Every value is exact in bf16."""
+    rng = np.random.default_rng(seed)
+    nb = K // 32
+    e = rng.integers(-20, 21, size=(M, nb, 1)).astype(np.float64)
+    k = rng.integers(-24, 25, size=(M, nb, 32)).astype(np.float64)
+    k[:, :, 0] = np.where(rng.random((M, nb)) < 0.5, 24.0, -24.0)
+    idx = np.argsort(rng.random((M, nb, 32)), axis=2)  # the 6 * 2^e element anywhere in the block
+    vals = np.take_along_axis(k, idx, axis=2) / 4.0 * np.exp2(e)
+    u = rng.random(vals.shape)
+    vals[u < 0.03] = -0.0
+    tiny = (u >= 0.03) & (u < 0.06)
+    vals[tiny] = np.where(rng.random(vals.shape) < 0.5, -1.0, 1.0)[tiny] * np.exp2(np.broadcast_to(e, vals.shape) - 12)[tiny]
+    kind = rng.random((M, nb))
+    vals[kind < 0.1] = rng.standard_normal((int((kind < 0.1).sum()), 32))
+    vals[(kind >= 0.1) & (kind < 0.15)] = 0.0
+    return torch.from_numpy(vals.reshape(M, K).astype(np.float32)).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("M", [37, 200])
+def test_fused_quantization_bitexact_through_identity(oracle_mod, M):
+    """With B = I (N = K) each output is one dequantized activation element,
+    exactly (a single non-zero product, no rounding in the sum, a value with at
+    most two significant bits in bf16), so the fused kernel's quantization is
+    checked bit for bit against the oracle at every block_m and split count."""
+    K = 512
+    A = grid_activation(M, K, seed=M)
+    B = torch.eye(K, dtype=torch.float32).to(torch.bfloat16)
+    _, _, W = quantized_weight(oracle_mod, B)
+    aq, as_ = oracle_mod.quantize(A)
+    expect = oracle_mod.dequantize(aq, as_)
+    assert np.array_equal(expect.astype(np.float32).astype(np.float64), expect)
+    Ad = A.cuda()
+    results = {"single fused kernel": mx.quant_gemm(Ad, W, workspace=torch.empty(0, dtype=torch.uint8, device="cuda"))}
+    for bm in (32, 64, 128, 256):
+        for splits in (1, 2):
+            plan = {"block_m": bm, "splits": splits, "stages": 1}
+            try:
+                results[f"fused plan {plan}"] = mx.gemm_with_plan(Ad, None, W, plan, True)
+            except mx.MXFP4Error as e:
+                assert e.status == 1 and bm == 256, plan  # only a 256-row tile may not fit in shared memory
+    assert len(results) >= 8
+    Aq, As = mx.quantize(Ad)
+    results["quantize + unfused"] = mx.gemm(Aq, As, W)
+    torch.cuda.synchronize()
+    for what, C in results.items():
+        got = C.float().cpu().numpy().astype(np.float64)
+        bad = got != expect
+        assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} differ, first at {np.argwhere(bad)[0]}"
+
+
 def test_gemm_every_plan_agrees(oracle_mod):
     M, N, K = 40, 384, 2048
     A, B = workloads.make_random(M, N, K, seed=99)
