@@ -314,8 +314,9 @@ def set_wait_timeout_ns(ns: int) -> None:
 
 def set_programmatic_launch(mode: int) -> None:
     """Overlap of a GEMM call with the kernel before it: 0 none, 1 set-up and
-    L2 prefetch only, 2 (default) also the weights into shared memory; see
-    mxfp4_set_programmatic_launch in include/mxfp4.h."""
+    L2 prefetch only, 2 also the weights into shared memory, 3 (default) as 2
+    with at most one grid running ahead; see mxfp4_set_programmatic_launch in
+    include/mxfp4.h."""
     _call("mxfp4_set_programmatic_launch", int(mode))
 
 

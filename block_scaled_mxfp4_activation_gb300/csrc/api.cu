@@ -4,6 +4,7 @@
 
 #include <atomic>
 #include <cstdio>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -14,7 +15,7 @@ namespace mxfp4 {
 namespace {
 
 std::atomic<uint64_t> g_timeout_ns{1000000000ull};
-std::atomic<int> g_programmatic{2};
+std::atomic<int> g_programmatic{3};
 
 // The CUDA error behind the last MXFP4_ERR_CUDA status of this thread.
 thread_local char g_last_error[256] = "";
@@ -124,6 +125,23 @@ bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, boo
   return r == CUDA_SUCCESS;
 }
 
+// 2-D map over the output C [M, N] bf16 for the TMA store of a whole
+// [block_m x 128] tile (no swizzle; rows past M and columns past N are not
+// written).  Needs N * 2 bytes per row to be a multiple of 16.
+bool encode_output_map(void* c, int64_t M, int64_t N, int block_m, CUtensorMap* map) {
+  if (N % 8 != 0) return false;
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return false;
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(N * 2)};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(block_m)};
+  cuuint32_t elem_strides[2] = {1, 1};
+  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box, elem_strides,
+                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // The default plan per (device, M, N, K, fused), computed once: the plan
 // search queries cluster occupancy, which is too slow for every call.
 void cached_default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
@@ -195,10 +213,13 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
     cached_default_plan(M, N, K, fused, dev->prop, &plan);
     if (plan.threads == 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   }
-  CUtensorMap map, amap;
+  CUtensorMap map, amap, cmap;
   if (!encode_weight_map(bpacked, N, K, &map)) return failure("cuTensorMapEncodeTiled (weights)");
   if (!encode_activation_map(a, M, K, fused ? lda : K / 2, fused, plan.block_m, &amap))
     return failure("cuTensorMapEncodeTiled (activation)");
+  // without a K split the output tile leaves by TMA store when a map can describe C
+  memset(&cmap, 0, sizeof(cmap));
+  const bool c_tma = plan.splits == 1 && encode_output_map(C, M, N, plan.block_m, &cmap);
   GemmArgs g{};
   g.a = a;
   g.a_scales = static_cast<const uint8_t*>(as);
@@ -226,9 +247,11 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   g.a_box_rows = activation_box_rows(M, plan.block_m);
   g.accumulators = plan.accumulators;
   g.weights_early = g_programmatic.load() >= 2 ? 1 : 0;
+  g.c_tma = c_tma ? 1 : 0;
+  g.trigger_late = g_programmatic.load() >= 3 ? 1 : 0;
   g.err = device_error_word();
   if (g.err == nullptr) return failure("cudaGetSymbolAddress (device error word)");
-  const cudaError_t e = launch_gemm(map, amap, g, plan, fused, g_programmatic.load() != 0, stream);
+  const cudaError_t e = launch_gemm(map, amap, cmap, g, plan, fused, g_programmatic.load() != 0, stream);
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("GEMM launch", e);
 }
 
@@ -405,7 +428,7 @@ mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns) {
 }
 
 mxfp4_status_t mxfp4_set_programmatic_launch(int mode) {
-  if (mode < 0 || mode > 2) return MXFP4_ERR_INVALID_ARG;
+  if (mode < 0 || mode > 3) return MXFP4_ERR_INVALID_ARG;
   g_programmatic.store(mode);
   return MXFP4_OK;
 }

@@ -72,7 +72,7 @@ __device__ __forceinline__ uint32_t sf_chunk_offset(int r) { return (r & 31) * 1
 template <int BM, bool kFused>
 __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
-                      const GemmArgs args) {
+                      const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
   using C = TileCfg<BM, kFused>;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -92,6 +92,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   const int n_tile = blockIdx.y, m_tile = blockIdx.z;
   const int m_base = m_tile * BM;
   const int m_valid = min(BM, args.M - m_base);
+  const int valid_blocks = 4 * ((m_valid + 15) >> 4);  // 32 x 16 output blocks holding rows below M
   const int kt_begin = static_cast<int>(rank) * args.kt_per_split;
   const int kt_end = min(args.k_tiles, kt_begin + args.kt_per_split);
   const int kt_count = max(0, kt_end - kt_begin);
@@ -113,6 +114,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tmap(&tmap_b);
     prefetch_tmap(&tmap_a);
+    if (args.c_tma) prefetch_tmap(&tmap_c);
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
@@ -125,11 +127,13 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
   const int nacc = args.accumulators;                 // independent accumulators (1, 2 or 4)
   const uint32_t tmem_sf = tmem_base + nacc * BM;     // scale columns follow the accumulators
 
-  // The next call in the stream may start its own prologue now.  Reads of data
-  // an earlier grid may write (the activation) and every global write come
-  // after grid_dependency_wait(); before it, only the weights (read-only for
-  // the lifetime of the call, by contract) and L2 prefetches.
-  grid_launch_dependents();
+  // The next call in the stream may start its own prologue now (or, with
+  // trigger_late, once every thread has passed its wait: at most one grid
+  // ahead).  Reads of data an earlier grid may write (the activation) and
+  // every global write come after grid_dependency_wait(); before it, only the
+  // weights (read-only for the lifetime of the call, by contract) and L2
+  // prefetches.
+  if (!args.trigger_late) grid_launch_dependents();
 
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
@@ -183,6 +187,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
       if (leader) tma_prefetch_l2_2d(&tmap_a, x, m_base);
     }
     grid_dependency_wait();
+    if (args.trigger_late) grid_launch_dependents();
     if (!args.weights_early)
       for (int i = 0; i < pre; ++i) issue_w(i);
     for (int i = 0; i < pre; ++i) issue_a(i);
@@ -211,6 +216,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     // instructions; the same lane issues every commit, which tracks that
     // lane's earlier operations.
     const bool leader = elect_one();
+    if (args.trigger_late) {
+      grid_dependency_wait();
+      grid_launch_dependents();
+    }
     for (int i = 0; i < kt_count; ++i) {
       const int s = i % stages, round = i / stages;
       const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
@@ -263,6 +272,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     // ------------------------------------------------------------------ activation producer
     const int tid = threadIdx.x - 64;
     grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
+    if (args.trigger_late) grid_launch_dependents();
     // fused: units of 16 bf16 (32 bytes), two per 32-element block; unit
     // u = tid + kAThreads * k is row u / 16, block (u / 2) % 8, half u % 2, so
     // warp w covers rows 2w + 16k and 2w + 16k + 1
@@ -371,11 +381,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
       if (lane == 0) mbar_arrive(full_a(s));
     }
 
-    // ------------------------------------------------------------------ epilogue: push partial blocks
-    // Block (chunk c of 16 activation rows, lane quarter qr) goes to cluster
-    // rank (4c + qr) % splits, into that CTA's slot [this rank][(4c + qr) / splits].
-    // The staging area is separate from the stage buffers, so a peer still
-    // running its MMAs is never disturbed.
+    // ------------------------------------------------------------------ epilogue
     const bool ok = mbar_wait(accum_bar, 0, timeout);
     if (!ok) report_error(args.err, kErrWaitAccum);
     tc_fence_after_sync();
@@ -403,9 +409,18 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
 #pragma unroll
         for (int e = 0; e < 16; ++e) r[e] = 0u;
       }
+      if (splits == 1 && args.c_tma) {
+        // no K split: bf16 into the output tile [BM rows][128 columns] at
+        // offset 0 (lane = column n, register e = row m; a warp's stores of
+        // one row are 64 contiguous bytes), sent by one TMA store below
+        __nv_bfloat16* cs = reinterpret_cast<__nv_bfloat16*>(smem) + (c * 16) * kTileN + qr * 32 + lane;
+#pragma unroll
+        for (int e = 0; e < 16; ++e) cs[e * kTileN] = __float2bfloat16_rn(__uint_as_float(r[e]));
+        continue;
+      }
       if (splits == 1) {
-        // no K split: bf16 straight from the accumulator registers to C
-        // (lane = weight row n, register e = activation row m)
+        // no K split and no TMA store (N not a multiple of 8): bf16 straight
+        // from the accumulator registers to C
         const int n = n_tile * kTileN + qr * 32 + lane;
         if (n < args.N) {
           __nv_bfloat16* col = args.c + static_cast<int64_t>(m_base) * args.N + n;
@@ -415,6 +430,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
         }
         continue;
       }
+      // K split: block (chunk c of 16 activation rows, lane quarter qr) goes
+      // to cluster rank (4c + qr) % splits, into that CTA's slot
+      // [this rank][(4c + qr) / splits].  The staging area is separate from
+      // the stage buffers, so a peer still running its MMAs is never disturbed.
       const int bi = 4 * c + qr;
       const uint32_t owner = static_cast<uint32_t>(bi % splits);
       const uint32_t dst = sbase + args.stg_off +
@@ -427,6 +446,14 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
         const uint32_t cdst = map_to_rank(dst, owner);
 #pragma unroll
         for (int e = 0; e < 16; ++e) st_cluster_f32(cdst + e * 128, __uint_as_float(r[e]));
+      }
+    }
+    if (splits == 1 && args.c_tma) {
+      fence_proxy_async_smem();        // the tile's generic stores, visible to the TMA engine
+      named_barrier(1, C::kAThreads);  // every epilogue warp has written its part
+      if (tid == 0) {
+        tma_store_2d(&tmap_c, n_tile * kTileN, m_base, sbase);
+        bulk_commit_group();
       }
     }
   }
@@ -443,7 +470,6 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     // Only local shared memory is read from here on, so no CTA waits for its
     // peers before exiting.
     const int tid = threadIdx.x - 64;
-    const int valid_blocks = 4 * ((m_valid + 15) >> 4);
     const int mine = (valid_blocks - static_cast<int>(rank) + splits - 1) / splits;
     const int n_base = n_tile * kTileN;
     const bool vec_ok = (args.N % 4) == 0;
@@ -476,12 +502,14 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
       }
     }
   }
+  // the output tile must stay in shared memory until the TMA store has read it
+  if (splits == 1 && args.c_tma && threadIdx.x == 64) bulk_wait_group_read0();
 }
 
 // ----------------------------------------------------------------------------- host side
 template <int BM, bool kFused>
-static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const GemmArgs& args,
-                            const mxfp4_plan_t& plan, bool programmatic, cudaStream_t s) {
+static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
+                            const GemmArgs& args, const mxfp4_plan_t& plan, bool programmatic, cudaStream_t s) {
   auto kernel = mxfp4_gemm_kernel<BM, kFused>;
   static int configured_device = -1;  // max dynamic smem set once per device
   int dev = 0;
@@ -506,15 +534,16 @@ static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a
   attr[1].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
   cfg.attrs = attr;
   cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, kernel, tmap_b, tmap_a, args);
+  return cudaLaunchKernelEx(&cfg, kernel, tmap_b, tmap_a, tmap_c, args);
 }
 
-cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const GemmArgs& args,
-                        const mxfp4_plan_t& plan, bool fused, bool programmatic, cudaStream_t s) {
-#define MXFP4_LAUNCH(BM_)                                                                     \
-  case BM_:                                                                                   \
-    return fused ? launch_t<BM_, true>(tmap_b, tmap_a, args, plan, programmatic, s)           \
-                 : launch_t<BM_, false>(tmap_b, tmap_a, args, plan, programmatic, s);
+cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
+                        const GemmArgs& args, const mxfp4_plan_t& plan, bool fused, bool programmatic,
+                        cudaStream_t s) {
+#define MXFP4_LAUNCH(BM_)                                                                       \
+  case BM_:                                                                                     \
+    return fused ? launch_t<BM_, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s)     \
+                 : launch_t<BM_, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);
   switch (plan.block_m) {
     MXFP4_LAUNCH(32)
     MXFP4_LAUNCH(64)
@@ -541,11 +570,14 @@ GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t 
   L.a_off = st * kTileN * kTileKBytes;
   L.abf_off = L.a_off + st * bm * kTileKBytes;
   L.sfw_off = L.abf_off + (fused ? st * bm * kTileK * 2 : 0u);
+  // without a K split the bf16 output tile is written over the operand
+  // buffers once the MMAs are done: keep room for it before the scales
+  if (splits == 1 && L.sfw_off < bm * kTileN * 2) L.sfw_off = bm * kTileN * 2;
   L.sfa_off = L.sfw_off + st * kSfTileBytes;
   L.stg_off = L.sfa_off + st * (bm > 128 ? 2u : 1u) * 2u * kSfChunkBytes;
   const int64_t rows = M < block_m ? M : block_m;
   const int blocks = static_cast<int>(4 * ceil_div(rows, 16));
-  L.stg_blocks = splits > 1 ? static_cast<int32_t>(ceil_div(blocks, splits)) : 0;  // no split: direct stores
+  L.stg_blocks = splits > 1 ? static_cast<int32_t>(ceil_div(blocks, splits)) : 0;  // no split: no staging
   L.bar_off = L.stg_off + static_cast<uint32_t>(splits * L.stg_blocks) * kBlockBytes;
   L.total = L.bar_off + (4 * st + 1) * 8 + 16;
   return L;
@@ -629,17 +661,19 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 #undef MXFP4_OCC
 }
 
-// The default plan.  Every call is latency-bound, so the plan maximises the
-// work in flight: as many CTAs as can be resident at once, up to two per SM
-// (two CTAs per SM keep twice the bytes in flight and quantize twice the
-// activation in parallel), all in a single wave.  Candidates: block_m from the
-// smallest tile that holds M (capped at 256) down to a quarter of it; every
-// split count that leaves no split empty; one or two stages (the ring wraps
-// when a split has more K tiles), or every K tile of the split when that
-// still fits.  Ties prefer the larger block_m (fewer re-reads of the weights),
-// then the larger stage count, then fewer splits.
+// The default plan.  Every call is latency-bound, so the plan minimises an
+// estimate of one CTA's critical path among the plans that run in a single
+// wave (every cluster resident at once, at most two CTAs per SM): each K tile
+// a split runs in sequence costs ~250 ns (operand loads, tensor-memory scale
+// copies, four MMAs) plus, on the fused kernel, ~200 ns per 32 activation rows
+// it quantizes; a K split adds ~700 ns for the cluster reduction (measured on
+// GB300 with graph-replayed calls).  Candidates: block_m from the smallest
+// tile that holds M (capped at 256) down to a quarter of it; every split count
+// that leaves no split empty; one or two stages, or every K tile of the split
+// when that still fits.  Ties prefer the larger block_m (fewer re-reads of the
+// weights), then the larger stage count, then fewer splits.
 // Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
-// the search below is not: sweeps of block_m x splits x stages, graph-replayed
+// the estimate is not: sweeps of block_m x splits x stages, graph-replayed
 // calls with rotating operands.  `fused` is the GEMM kernel's kind (the large-M
 // shapes run the pre-quantized kernel on the fused entry's two-pass route).
 struct TunedPlan {
@@ -652,6 +686,13 @@ constexpr TunedPlan kTunedPlans[] = {
     {64, 7168, 2048, false, 64, 4, 2},
     {256, 3072, 1536, false, 64, 2, 3},
 };
+
+// Estimated critical path of one CTA, in ns (see above).
+static int64_t plan_cost_ns(const mxfp4_plan_t& p, int64_t M, bool fused) {
+  const int64_t rows = M < p.block_m ? M : p.block_m;
+  const int64_t tile = 250 + (fused ? 200 * ceil_div(rows, 32) : 0);
+  return p.k_tiles_per_split * tile + (p.splits > 1 ? 700 : 0);
+}
 
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                   mxfp4_plan_t* p) {
@@ -686,8 +727,8 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
         if (!finish_plan(M, N, K, fused, prop, &q) || q.stages != st) continue;
         const int64_t clusters = static_cast<int64_t>(q.grid_y) * q.grid_z;
         const int64_t ctas = clusters * splits;
-        const int64_t one_wave = clusters <= active_clusters(q, fused) ? 1 : 0;
-        const int64_t score[5] = {one_wave, ctas <= cap ? ctas : -ctas, bm, st, -splits};
+        const int64_t one_wave = ctas <= cap && clusters <= active_clusters(q, fused) ? 1 : 0;
+        const int64_t score[5] = {one_wave, one_wave ? -plan_cost_ns(q, M, fused) : -ctas, bm, st, -splits};
         bool better = false;
         for (int i = 0; i < 5; ++i) {
           if (score[i] != best[i]) {

@@ -62,12 +62,17 @@ struct GemmArgs {
   int32_t stg_blocks;       // 32 x 16 partial blocks each CTA may receive from one split
   int32_t a_box_rows;       // rows of one activation TMA box: min(block_m, roundup(M, 8))
   int32_t accumulators;     // independent fp32 accumulator tiles in tensor memory (1, 2, 4)
+  int32_t c_tma;            // no K split: C leaves through a bf16 tile in shared memory and one TMA store
+  int32_t trigger_late;     // let the next grid launch only once this grid has passed its own wait
 };
 
 // Shared-memory layout of one GEMM CTA (byte offsets from a 1024-aligned base):
 // weight code tiles, activation code tiles, bf16 activation staging (fused),
 // weight scales, activation scales (one of each per stage), the split-K
 // staging slots ([splits][stg_blocks] blocks of 2 KB), then the mbarriers.
+// Without a K split the bf16 output tile [block_m][128] is staged at offset 0
+// once the MMAs are done (the operand buffers are free by then); the layout
+// keeps at least block_m x 256 bytes before the scales for it.
 struct GemmLayout {
   uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off, total;
   int32_t stg_blocks;
@@ -91,8 +96,9 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
                  mxfp4_plan_t* plan);
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                   mxfp4_plan_t* plan);
-cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const GemmArgs& args,
-                        const mxfp4_plan_t& plan, bool fused, bool programmatic, cudaStream_t s);
+cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
+                        const GemmArgs& args, const mxfp4_plan_t& plan, bool fused, bool programmatic,
+                        cudaStream_t s);
 
 cudaError_t read_device_error(cudaStream_t s, uint32_t* code, bool reset);
 // Sets the calling thread's message for mxfp4_last_error_string().

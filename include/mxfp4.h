@@ -234,13 +234,19 @@ mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns);
  *   1  the GEMM may start early, but until the previous kernel has completed
  *      it only sets up and prefetches its weight and activation bytes into L2
  *      (L2 is coherent, so this never reads stale data);
- *   2  (default) as 1, and the weight codes and scales are also loaded into
- *      shared memory before the previous kernel has completed.  Contract: the
- *      packed weight buffer is not written by the kernel that immediately
- *      precedes the GEMM on its stream (weights are read-only parameters; none
- *      of this library's kernels writes a weight buffer it is not given as an
- *      output, and a kernel that does not use programmatic launch has always
- *      completed before the GEMM starts).
+ *   2  as 1, and the weight codes and scales are also loaded into shared
+ *      memory before the previous kernel has completed.  Contract: the packed
+ *      weight buffer is not written by the kernel that immediately precedes
+ *      the GEMM on its stream (weights are read-only parameters; none of this
+ *      library's kernels writes a weight buffer it is not given as an output,
+ *      and a kernel that does not use programmatic launch has always
+ *      completed before the GEMM starts).  A GEMM lets the next kernel start
+ *      as soon as it has itself started, so a chain of calls can run several
+ *      grids ahead;
+ *   3  (default) as 2, but a GEMM lets the next kernel start only once its
+ *      own wait for the previous kernel has ended: at most one grid runs
+ *      ahead, and the grids waiting early no longer crowd the running one's
+ *      SMs (measured faster on GB300 for every shape with few K tiles).
  * mxfp4_quantize follows modes 1 and 2 likewise: it may start early, but reads
  * A and writes its outputs only after the previous kernel has completed.
  * In every mode the activation is read, and C written, only after the
