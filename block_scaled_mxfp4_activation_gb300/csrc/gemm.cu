@@ -69,8 +69,60 @@ __device__ __forceinline__ uint32_t mxf4_idesc(uint32_t scale_id) {
 // Byte offset of scale j (0..3) of row r in a 128-row x 4-scale chunk.
 __device__ __forceinline__ uint32_t sf_chunk_offset(int r) { return (r & 31) * 16 + ((r & 127) >> 5) * 4; }
 
+// Quantizes one staged bf16 activation tile [BM rows][256] (512-byte rows) into
+// the MMA operand's codes (128-byte rows, 128-byte swizzle) and the scale
+// chunks, with the kAThreads producer threads: two lanes per 32-element block
+// (16 bf16 each), unit u = tid + kAThreads * k is row u / 16, block (u / 2) % 8,
+// half u % 2, so warp w covers rows 2w + 16k and 2w + 16k + 1.  kGuard: rows
+// past m_valid are skipped (a whole warp's unit at once, so the pair shuffle
+// stays convergent; their output columns are never stored).
+template <int BM, int kThreads, int kRowChunks, bool kGuard>
+__device__ __forceinline__ void quantize_tile(const uint8_t* abf, uint8_t* a_tile, uint8_t* sfa, int tid, int m_valid) {
+  constexpr int kUnits = BM * 16 / kThreads;
+  const int lane = tid & 31, pw = tid >> 5;
+  const int rot = (lane >> 2) & 1;  // which half of its 32 bytes a lane loads first: no bank conflicts
+  const int half = lane & 1;        // which 16 elements of the block the lane owns
+  // (batches of at most 4 units, 2 at block_m >= 128, to fit the register
+  // budget of two CTAs per SM)
+  constexpr int kBatch = kUnits < (BM < 128 ? 4 : 2) ? kUnits : (BM < 128 ? 4 : 2);
+#pragma unroll(BM < 256 ? kUnits / kBatch : 1)
+  for (int k0 = 0; k0 < kUnits; k0 += kBatch) {
+    uint4 v[kBatch][2];  // all loads of a batch first, then the independent chains
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      const uint8_t* src = abf + (tid + (k0 + e) * kThreads) * 32;
+      if (!kGuard || 2 * pw + 16 * (k0 + e) < m_valid) {
+        v[e][0] = *reinterpret_cast<const uint4*>(src + 16 * rot);  // 16 bytes rot, then 16 bytes rot ^ 1
+        v[e][1] = *reinterpret_cast<const uint4*>(src + 16 * (rot ^ 1));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      if (kGuard && 2 * pw + 16 * (k0 + e) >= m_valid) continue;  // warp-uniform
+      const int u = tid + (k0 + e) * kThreads;
+      const int m = u >> 4, b = (u >> 1) & 7;
+      uint32_t amax = absmax16_bf16(v[e][0], v[e][1]);
+      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      const uint32_t byte = scale_byte_from_amax(amax);
+      const uint16_t sbf = scale_bf16_from_byte(byte);
+      uint32_t w0 = e2m1_pack8(v[e][0], sbf), w1 = e2m1_pack8(v[e][1], sbf);
+      if (rot) {  // back to memory order
+        const uint32_t t = w0;
+        w0 = w1;
+        w1 = t;
+      }
+      if (!kGuard || m < m_valid) {
+        *reinterpret_cast<uint2*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + 8 * half) = make_uint2(w0, w1);
+        if (half == 0)
+          sfa[((b >> 2) * kRowChunks + (m >> 7)) * kSfChunkBytes + sf_chunk_offset(m) + (b & 3)] =
+              static_cast<uint8_t>(byte);
+      }
+    }
+  }
+}
+
 template <int BM, bool kFused>
-__global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
+__global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
   using C = TileCfg<BM, kFused>;
@@ -273,16 +325,6 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
     const int tid = threadIdx.x - 64;
     grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
     if (args.trigger_late) grid_launch_dependents();
-    // fused: units of 16 bf16 (32 bytes), two per 32-element block; unit
-    // u = tid + kAThreads * k is row u / 16, block (u / 2) % 8, half u % 2, so
-    // warp w covers rows 2w + 16k and 2w + 16k + 1
-    constexpr int kUnits = BM * 16 / C::kAThreads;
-    // (batches of up to 4 units below block_m 128, 2 above: registers stay under
-    // 102 per thread, so two CTAs fit on an SM)
-    constexpr int kBatch = kUnits < (BM < 128 ? 4 : 2) ? kUnits : (BM < 128 ? 4 : 2);
-    const int pw = tid >> 5;
-    const int rot = (lane >> 2) & 1;  // which half of its 32 bytes a lane loads first: no bank conflicts
-    const int half = lane & 1;        // which 16 elements of the block the lane owns
     const int64_t nblk = args.K / 32;
     // unfused: the 8 scale bytes of row `tid` for K tile i (one row per thread;
     // block_m <= 256 = the producer thread count)
@@ -319,41 +361,11 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 1)
       uint8_t* a_tile = smem + args.a_off + s * C::kATileBytes;
       uint8_t* sfa = smem + args.sfa_off + s * C::kSfaStageBytes;
       if constexpr (kFused) {
-        // Quantize the staged bf16 tile (256 bf16 = 512 bytes per row): each
-        // lane pair shares a block's maximum through one shuffle; a warp
-        // skips a unit whose two rows are both past M (their output columns
-        // are never stored).
         const uint8_t* abf = smem + args.abf_off + s * C::kAbfBytes;
-#pragma unroll(BM < 256 ? kUnits : 1)
-        for (int k0 = 0; k0 < kUnits; k0 += kBatch) {
-          uint4 v[kBatch][2];  // all loads of a batch first, then the independent chains
-#pragma unroll
-          for (int e = 0; e < kBatch; ++e) {
-            const uint8_t* src = abf + (tid + (k0 + e) * C::kAThreads) * 32;
-            if (2 * pw + 16 * (k0 + e) < m_valid) {
-              v[e][0] = *reinterpret_cast<const uint4*>(src + 16 * rot);  // 16 bytes rot, then 16 bytes rot ^ 1
-              v[e][1] = *reinterpret_cast<const uint4*>(src + 16 * (rot ^ 1));
-            }
-          }
-#pragma unroll
-          for (int e = 0; e < kBatch; ++e) {
-            if (2 * pw + 16 * (k0 + e) >= m_valid) continue;  // warp-uniform
-            const int u = tid + (k0 + e) * C::kAThreads;
-            const int m = u >> 4, b = (u >> 1) & 7;
-            uint32_t amax = absmax16_bf16(v[e][0], v[e][1]);
-            amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            const uint32_t byte = scale_byte_from_amax(amax);
-            const uint16_t sbf = scale_bf16_from_byte(byte);
-            const uint32_t c0 = e2m1_pack8(v[e][0], sbf), c1 = e2m1_pack8(v[e][1], sbf);
-            const uint32_t w0 = rot ? c1 : c0, w1 = rot ? c0 : c1;  // back to memory order
-            if (m < m_valid) {
-              *reinterpret_cast<uint2*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + 8 * half) = make_uint2(w0, w1);
-              if (half == 0)
-                sfa[((b >> 2) * C::kRowChunks + (m >> 7)) * kSfChunkBytes + sf_chunk_offset(m) + (b & 3)] =
-                    static_cast<uint8_t>(byte);
-            }
-          }
-        }
+        if (m_valid >= BM)
+          quantize_tile<BM, C::kAThreads, C::kRowChunks, false>(abf, a_tile, sfa, tid, m_valid);
+        else
+          quantize_tile<BM, C::kAThreads, C::kRowChunks, true>(abf, a_tile, sfa, tid, m_valid);
       } else {
         // Pre-quantized activation: the codes arrived by TMA; place the
         // natural [M, K/32] scales into the chunk layout, one row per thread
