@@ -180,8 +180,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   const uint32_t tmem_sf = tmem_base + nacc * BM;     // scale columns follow the accumulators
 
   // The next call in the stream may start its own prologue now (or, with
-  // trigger_late, once every thread has passed its wait: at most one grid
-  // ahead).  Reads of data an earlier grid may write (the activation) and
+  // trigger_late, once this grid's activation loads are under way: at most
+  // one grid ahead, and its prologue's weight loads do not queue in front of
+  // this grid's activation loads).  Reads of data an earlier grid may write (the activation) and
   // every global write come after grid_dependency_wait(); before it, only the
   // weights (read-only for the lifetime of the call, by contract) and L2
   // prefetches.
@@ -239,10 +240,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       if (leader) tma_prefetch_l2_2d(&tmap_a, x, m_base);
     }
     grid_dependency_wait();
-    if (args.trigger_late) grid_launch_dependents();
     if (!args.weights_early)
       for (int i = 0; i < pre; ++i) issue_w(i);
     for (int i = 0; i < pre; ++i) issue_a(i);
+    if (args.trigger_late) grid_launch_dependents();
     int issued = pre;
     for (int i = pre; i < kt_count; ++i) {
       const int s = i % stages, round = i / stages;
@@ -268,10 +269,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     // instructions; the same lane issues every commit, which tracks that
     // lane's earlier operations.
     const bool leader = elect_one();
-    if (args.trigger_late) {
-      grid_dependency_wait();
-      grid_launch_dependents();
-    }
+    bool triggered = !args.trigger_late;
     for (int i = 0; i < kt_count; ++i) {
       const int s = i % stages, round = i / stages;
       const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
@@ -298,6 +296,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         *abort_flag = 1u;
       }
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+      if (!triggered) {  // the activation has landed: the next grid may start
+        grid_launch_dependents();
+        triggered = true;
+      }
       tc_fence_after_sync();
       if (leader) {
 #pragma unroll
@@ -319,12 +321,13 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       __syncwarp();
     }
     if (leader) tc_commit(accum_bar);  // always: the epilogue waits on it
+    if (!triggered) grid_launch_dependents();
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ activation producer
     const int tid = threadIdx.x - 64;
     grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
-    if (args.trigger_late) grid_launch_dependents();
+    bool triggered = !args.trigger_late;
     const int64_t nblk = args.K / 32;
     // unfused: the 8 scale bytes of row `tid` for K tile i (one row per thread;
     // block_m <= 256 = the producer thread count)
@@ -356,6 +359,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       if (!*abort_flag && !mbar_wait(full_in(s), round & 1, timeout)) {
         report_error(args.err, kErrWaitTma);
         *abort_flag = 1u;
+      }
+      if (!triggered) {  // the activation tile has landed: the next grid may start
+        grid_launch_dependents();
+        triggered = true;
       }
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;  // warp-uniform: the shuffles below need every lane
       uint8_t* a_tile = smem + args.a_off + s * C::kATileBytes;
@@ -393,6 +400,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       if (lane == 0) mbar_arrive(full_a(s));
     }
 
+    if (!triggered) grid_launch_dependents();
     // ------------------------------------------------------------------ epilogue
     const bool ok = mbar_wait(accum_bar, 0, timeout);
     if (!ok) report_error(args.err, kErrWaitAccum);

@@ -244,9 +244,10 @@ mxfp4_status_t mxfp4_set_wait_timeout_ns(uint64_t ns);
  *      as soon as it has itself started, so a chain of calls can run several
  *      grids ahead;
  *   3  (default) as 2, but a GEMM lets the next kernel start only once its
- *      own wait for the previous kernel has ended: at most one grid runs
- *      ahead, and the grids waiting early no longer crowd the running one's
- *      SMs (measured faster on GB300 for every shape with few K tiles).
+ *      own wait for the previous kernel has ended and its activation loads
+ *      are under way: at most one grid runs ahead, and the grids waiting
+ *      early no longer crowd the running one's SMs (measured faster on GB300
+ *      for every shape with few K tiles).
  * mxfp4_quantize follows modes 1 and 2 likewise: it may start early, but reads
  * A and writes its outputs only after the previous kernel has completed.
  * In every mode the activation is read, and C written, only after the
