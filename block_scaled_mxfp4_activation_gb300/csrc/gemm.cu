@@ -330,10 +330,18 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     bool triggered = !args.trigger_late;
     const int64_t nblk = args.K / 32;
     // unfused: the 8 scale bytes of row `tid` for K tile i (one row per thread;
-    // block_m <= 256 = the producer thread count)
+    // block_m <= 256 = the producer thread count): one 8-byte load when rows
+    // are 8-byte aligned (K a multiple of 256), else byte by byte
+    const bool scales_vec8 = nblk % 8 == 0 && (reinterpret_cast<uintptr_t>(args.a_scales) & 7u) == 0;
     auto load_scales = [&](int i, uint32_t& w0, uint32_t& w1) {
       const int64_t j0 = static_cast<int64_t>(kt_begin + i) * 8;
       const uint8_t* src = args.a_scales + static_cast<int64_t>(m_base + tid) * nblk + j0;
+      if (scales_vec8) {
+        const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+        w0 = v.x;
+        w1 = v.y;
+        return;
+      }
       uint32_t w[2] = {0u, 0u};
 #pragma unroll
       for (int jb = 0; jb < 8; ++jb)
