@@ -270,6 +270,64 @@ def test_gemm_deterministic_and_graph_replay(oracle_mod):
     assert torch.equal(out, C1)
 
 
+@pytest.mark.parametrize("M", [32, 64])
+def test_chained_layers_under_every_overlap_mode(oracle_mod, M):
+    """Layer i's output is layer i+1's activation (square 512 x 512 layers), so
+    every call reads what the call before it wrote while programmatic launch
+    lets it start early.  Each overlap mode, eager and graph-replayed, must give
+    exactly the result of mode 0 (no overlap); M = 64 runs the two-pass route
+    (quantize into a shared workspace, then the GEMM), M = 32 the fused kernel.
+    The first layer is also checked against the oracle."""
+    D, layers = 512, 6
+    rng = np.random.default_rng(M)
+    Ws = []
+    for _ in range(layers):
+        B = torch.from_numpy((rng.standard_normal((D, D)) / np.sqrt(D)).astype(np.float32)).to(torch.bfloat16)
+        Ws.append(quantized_weight(oracle_mod, B)[2])
+    A0 = torch.from_numpy(rng.standard_normal((M, D)).astype(np.float32)).to(torch.bfloat16).cuda()
+    ws = torch.empty(max(mx.workspace_bytes(M, D, D), 1), dtype=torch.uint8, device="cuda")
+    outs = [torch.empty((M, D), dtype=torch.bfloat16, device="cuda") for _ in range(layers)]
+
+    def chain():
+        x = A0
+        for W, o in zip(Ws, outs):
+            mx.quant_gemm(x, W, out=o, workspace=ws)
+            x = o
+        return x
+
+    try:
+        mx.set_programmatic_launch(0)
+        ref = chain().clone()
+        torch.cuda.synchronize()
+        for mode in (1, 2, 3):
+            mx.set_programmatic_launch(mode)
+            for o in outs:
+                o.fill_(float("nan"))
+            got = chain()
+            torch.cuda.synchronize()
+            assert torch.equal(got, ref), f"eager chain, mode {mode}"
+            s = torch.cuda.Stream()
+            s.wait_stream(torch.cuda.current_stream())
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.stream(s), torch.cuda.graph(g, stream=s):
+                chain()
+            for o in outs:
+                o.fill_(float("nan"))
+            torch.cuda.synchronize()
+            for _ in range(3):
+                g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(outs[-1], ref), f"graph-replayed chain, mode {mode}"
+    finally:
+        mx.set_programmatic_launch(3)
+    # layer 0 against the oracle (the later layers differ only in their inputs)
+    bq, bs, _ = quantized_weight(oracle_mod, torch.from_numpy(
+        (np.random.default_rng(M).standard_normal((D, D)) / np.sqrt(D)).astype(np.float32)).to(torch.bfloat16))
+    _, _, c64, _ = oracle_mod.quant_gemm(A0.cpu(), bq, bs)
+    mx.set_programmatic_launch(3)
+    check_close(mx.quant_gemm(A0, Ws[0]), c64, f"first layer, M={M}")
+
+
 # ----------------------------------------------------------------------------- GEMM, full sizes
 @pytest.mark.parametrize("name", list(workloads.WORKLOADS))
 def test_gemm_full_size_sampled(oracle_mod, name):
