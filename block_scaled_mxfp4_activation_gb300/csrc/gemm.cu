@@ -695,11 +695,16 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // a split runs in sequence costs ~250 ns (operand loads, tensor-memory scale
 // copies, four MMAs) plus, on the fused kernel, ~200 ns per 32 activation rows
 // it quantizes; a K split adds ~700 ns for the cluster reduction (measured on
-// GB300 with graph-replayed calls).  Candidates: block_m from the smallest
-// tile that holds M (capped at 256) down to a quarter of it; every split count
-// that leaves no split empty; one or two stages, or every K tile of the split
-// when that still fits.  Ties prefer the larger block_m (fewer re-reads of the
-// weights), then the larger stage count, then fewer splits.
+// GB300 with graph-replayed calls).  Among plans that run in one wave, those
+// whose shared memory lets two CTAs share an SM come first: the next call's
+// CTAs then start early beside this call's (programmatic launch), and losing
+// that overlap costs more than any stage depth gains (K = 7168, 7 splits: 2
+// stages 5.6 us, 4 stages with one CTA per SM 10.0 us).  Candidates: block_m
+// from the smallest tile that holds M (capped at 256) down to a quarter of it;
+// every split count that leaves no split empty; one or two stages, or every K
+// tile of the split when that still fits.  Ties prefer the larger block_m
+// (fewer re-reads of the weights), then the larger stage count, then fewer
+// splits.
 // Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
 // the estimate is not: sweeps of block_m x splits x stages, graph-replayed
 // calls with rotating operands.  `fused` is the GEMM kernel's kind (the large-M
@@ -741,7 +746,7 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
   const int bm0 = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   const int64_t k_tiles = ceil_div(K, kTileK);
   const int64_t cap = 2 * static_cast<int64_t>(prop.multiProcessorCount);
-  int64_t best[5] = {-1, 0, 0, 0, 0};
+  int64_t best[6] = {-1, 0, 0, 0, 0, 0};
   for (int bm = bm0; bm >= 32 && bm * 4 >= bm0; bm /= 2) {
     for (int64_t splits = 1; splits <= kMaxSplits && splits <= k_tiles; ++splits) {
       const int64_t per = ceil_div(k_tiles, splits);
@@ -756,16 +761,21 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
         const int64_t clusters = static_cast<int64_t>(q.grid_y) * q.grid_z;
         const int64_t ctas = clusters * splits;
         const int64_t one_wave = ctas <= cap && clusters <= active_clusters(q, fused) ? 1 : 0;
-        const int64_t score[5] = {one_wave, one_wave ? -plan_cost_ns(q, M, fused) : -ctas, bm, st, -splits};
+        // two CTAs per SM leave room for the next call's CTAs to start early
+        const int64_t two_per_sm =
+            2 * (static_cast<int64_t>(q.smem_bytes) + prop.reservedSharedMemPerBlock) <= prop.sharedMemPerMultiprocessor
+                ? 1
+                : 0;
+        const int64_t score[6] = {one_wave, two_per_sm, one_wave ? -plan_cost_ns(q, M, fused) : -ctas, bm, st, -splits};
         bool better = false;
-        for (int i = 0; i < 5; ++i) {
+        for (int i = 0; i < 6; ++i) {
           if (score[i] != best[i]) {
             better = score[i] > best[i];
             break;
           }
         }
         if (better) {
-          for (int i = 0; i < 5; ++i) best[i] = score[i];
+          for (int i = 0; i < 6; ++i) best[i] = score[i];
           *p = q;
         }
       }
