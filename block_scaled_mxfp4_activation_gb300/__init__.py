@@ -106,17 +106,26 @@ def status_string(status: int) -> str:
         return "?"
 
 
-def _stream(stream=None) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return int(s.cuda_stream)
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+
+
+def _stream(stream=None, device: torch.device | None = None) -> int:
+    """The CUDA stream handle to launch on: `stream`, else torch's current
+    stream of `device` (or of the current device)."""
+    if stream is not None:
+        return int(stream.cuda_stream)
+    if _raw_stream is not None:  # the handle without building a Stream object
+        idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
+        return int(_raw_stream(idx))
+    return int(torch.cuda.current_stream().cuda_stream)
 
 
 def _ptr(t: torch.Tensor | None):
-    return None if t is None else ctypes.c_void_p(t.data_ptr())
+    return None if t is None else t.data_ptr()  # c_void_p argtypes take the integer address
 
 
 def _call(name: str, *args):
-    lib = load_library()
+    lib = _lib if _lib is not None else load_library()
     status = getattr(lib, name)(*args)
     if status != MXFP4_OK:
         detail = lib.mxfp4_last_error_string().decode() if status == 5 else ""
@@ -139,7 +148,7 @@ def quantize(A: torch.Tensor, out: tuple[torch.Tensor, torch.Tensor] | None = No
         out = (torch.empty((M, K // 2), dtype=torch.uint8, device=A.device),
                torch.empty((M, K // 32), dtype=torch.uint8, device=A.device))
     Aq, As = out
-    _call("mxfp4_quantize", _ptr(A), M, K, A.stride(0), _ptr(Aq), _ptr(As), _stream(stream))
+    _call("mxfp4_quantize", _ptr(A), M, K, A.stride(0), _ptr(Aq), _ptr(As), _stream(stream, A.device))
     return Aq, As
 
 
@@ -205,8 +214,15 @@ def quantize_weights(B: torch.Tensor, stream=None) -> PackedWeight:
 
 
 # ----------------------------------------------------------------------------- GEMM
+_ws_bytes: dict = {}
+
+
 def workspace_bytes(M: int, N: int, K: int) -> int:
-    return int(load_library().mxfp4_workspace_bytes(M, N, K))
+    key = (M, N, K)
+    v = _ws_bytes.get(key)
+    if v is None:
+        v = _ws_bytes[key] = int(load_library().mxfp4_workspace_bytes(M, N, K))
+    return v
 
 
 def _weight(W: PackedWeight) -> PackedWeight:
@@ -226,7 +242,7 @@ def gemm(Aq: torch.Tensor, As: torch.Tensor, W: PackedWeight, out: torch.Tensor 
         raise ValueError("Aq/As shapes do not match the weight's K")
     if out is None:
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=Aq.device)
-    _call("mxfp4_gemm", _ptr(Aq), _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K, None, 0, _stream(stream))
+    _call("mxfp4_gemm", _ptr(Aq), _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K, None, 0, _stream(stream, Aq.device))
     return out
 
 
@@ -250,7 +266,7 @@ def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=A.device)
     ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel()) if workspace is not None else (None, 0)
     _call("mxfp4_quant_gemm", _ptr(A), A.stride(0), _ptr(W.data), _ptr(out), M, W.N, W.K, ws_ptr, ws_bytes,
-          _stream(stream))
+          _stream(stream, A.device))
     return out
 
 
@@ -266,7 +282,7 @@ def quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, 
     M = A_host.shape[0]
     ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel()) if workspace is not None else (None, 0)
     _call("mxfp4_quant_gemm_host", _ptr(A_host), A_host.stride(0), _ptr(A_dev), A_dev.stride(0), _ptr(W.data),
-          _ptr(C_dev), _ptr(C_host), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream))
+          _ptr(C_dev), _ptr(C_host), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream, A_dev.device))
     return C_host
 
 

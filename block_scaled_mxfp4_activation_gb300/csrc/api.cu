@@ -32,6 +32,17 @@ mxfp4_status_t failure(const char* what) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The device's address of pinned, mapped host memory (null for anything else:
+// pageable or device memory, or a pointer CUDA does not know).
+const void* device_view(const void* host_ptr) {
+  cudaPointerAttributes a;
+  if (cudaPointerGetAttributes(&a, host_ptr) != cudaSuccess) {
+    cudaGetLastError();  // not a CUDA error the caller should see
+    return nullptr;
+  }
+  return a.type == cudaMemoryTypeHost ? a.devicePointer : nullptr;
+}
+
 struct DeviceInfo {
   bool ok = false;
   cudaDeviceProp prop{};
@@ -367,13 +378,29 @@ mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void*
   if (!aligned16(A_dev) || !aligned16(Bpacked) || !aligned16(C_dev) || lda_dev % 8 != 0)
     return MXFP4_ERR_MISALIGNED;
   if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-  if (current_device(&st) == nullptr) return st;
-  cudaError_t e = cudaMemcpy2DAsync(A_dev, static_cast<size_t>(lda_dev) * 2, A_host, static_cast<size_t>(lda_host) * 2,
-                                    static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
+  const DeviceInfo* dev = current_device(&st);
+  if (dev == nullptr) return st;
+  const bool programmatic = g_programmatic.load() != 0;
+  const int sms = dev->prop.multiProcessorCount;
+  // Pinned, mapped host buffers are moved by SM threads over the host link;
+  // anything else (pageable memory, unaligned rows) by the copy engines.
+  const void* a_src = device_view(A_host);
+  cudaError_t e;
+  if (a_src != nullptr && aligned16(a_src) && lda_host % 8 == 0) {
+    e = launch_copy_rows(a_src, lda_host * 2, A_dev, lda_dev * 2, K * 2, M, true, programmatic, sms, s);
+  } else {
+    e = cudaMemcpy2DAsync(A_dev, static_cast<size_t>(lda_dev) * 2, A_host, static_cast<size_t>(lda_host) * 2,
+                          static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
+  }
   if (e != cudaSuccess) return cuda_failure("activation upload", e);
   st = mxfp4_quant_gemm(A_dev, lda_dev, Bpacked, C_dev, M, N, K, ws, ws_bytes, stream);
   if (st != MXFP4_OK) return st;
-  e = cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(M) * static_cast<size_t>(N) * 2, cudaMemcpyDeviceToHost, s);
+  const int64_t c_bytes = M * N * 2;
+  void* c_dst = const_cast<void*>(device_view(C_host));
+  if (c_dst != nullptr && aligned16(c_dst) && c_bytes % 16 == 0)
+    e = launch_copy_rows(C_dev, c_bytes, c_dst, c_bytes, c_bytes, 1, false, programmatic, sms, s);
+  else
+    e = cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(c_bytes), cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("result download", e);
 }
 

@@ -86,6 +86,10 @@ cudaError_t launch_pack_weights(const void* Bq, const void* Bs, int64_t N, int64
                                 cudaStream_t s);
 cudaError_t launch_pack_from_shuffled(const void* Bsh, const void* Ssh, int64_t N, int64_t K, void* Bp,
                                       cudaStream_t s);
+// Row copy by SM threads between device-addressable buffers (row_bytes, pitches
+// and addresses multiples of 16); see host_copy.cu.
+cudaError_t launch_copy_rows(const void* src, int64_t src_pitch, void* dst, int64_t dst_pitch, int64_t row_bytes,
+                             int64_t rows, bool src_early, bool programmatic, int sm_count, cudaStream_t s);
 cudaError_t launch_unpack_weights(const void* Bp, int64_t N, int64_t K, void* Bq, void* Bs,
                                   cudaStream_t s);
 cudaError_t launch_diag_wait(uint64_t timeout_ns, cudaStream_t s);

@@ -351,20 +351,37 @@ def test_gemm_full_size_sampled(oracle_mod, name):
         assert torch.equal(C, C_unfused)
 
 
-def test_quant_gemm_host_buffers(oracle_mod):
-    for M, N, K, lda in ((32, 512, 512, 520), (64, 384, 1024, 1024)):
-        A, B = workloads.make_random(M, N, K, seed=M + K)
-        Ah = torch.zeros((M, lda), dtype=torch.bfloat16)
-        Ah[:, :K] = A
-        Ah = Ah.pin_memory()[:, :K]
-        W = mx.quantize_weights(B.cuda())
+@pytest.mark.parametrize("pinned", [True, False])
+def test_quant_gemm_host_buffers(oracle_mod, pinned):
+    """Host activation in, host result out, one call: pinned buffers go through
+    the library's SM copy kernel, pageable ones through cudaMemcpy; row pitches
+    that break 16-byte alignment (lda 516) take the copy engines too.  Several
+    calls back to back with different inputs and no synchronisation between
+    them, every result checked (a copy reading too early or writing too late
+    shows as a stale or torn result)."""
+    for M, N, K, lda in ((32, 512, 512, 520), (64, 384, 1024, 1024), (5, 264, 512, 516), (3, 131, 256, 256)):
+        W = mx.quantize_weights(workloads.make_random(M, N, K, seed=M + K)[1].cuda())
         Ad = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
         Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
-        Ch = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
-        mx.quant_gemm_host(Ah, W, Ad, Cd, Ch)
+        calls = 4
+        hosts_A, hosts_C, expect = [], [], []
+        for c in range(calls):
+            A = workloads.make_random(M, N, K, seed=100 * c + M + K)[0]
+            Ah = torch.zeros((M, lda), dtype=torch.bfloat16)
+            Ah[:, :K] = A
+            Ch = torch.full((M, N), float("nan"), dtype=torch.bfloat16)
+            if pinned:
+                Ah, Ch = Ah.pin_memory(), Ch.pin_memory()
+            hosts_A.append(Ah[:, :K])
+            hosts_C.append(Ch)
+            expect.append(mx.quant_gemm(A.cuda(), W).cpu())
         torch.cuda.synchronize()
-        assert torch.equal(Ad.cpu(), A)
-        assert torch.equal(Ch, mx.quant_gemm(A.cuda(), W).cpu())
+        for c in range(calls):
+            mx.quant_gemm_host(hosts_A[c], W, Ad, Cd, hosts_C[c])
+        torch.cuda.synchronize()
+        assert torch.equal(Ad.cpu(), hosts_A[-1].contiguous())
+        for c in range(calls):
+            assert torch.equal(hosts_C[c], expect[c]), f"M={M} N={N} K={K} lda={lda} call {c}"
 
 
 # ----------------------------------------------------------------------------- bounded waits
