@@ -84,21 +84,55 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
+// Encodes a 2-D tiled tensor map (element strides 1, no interleave, L2
+// promotion 256 B, no OOB fill), reusing the result of an identical earlier
+// request from this thread: a map holds only the address, shape, strides and
+// box, so repeated calls on the same buffers (every layer call, every step of
+// a loop) skip the encoder.  A small round-robin cache per thread.
+bool encode_2d(CUtensorMapDataType type, const void* base, uint64_t dim0, uint64_t dim1, uint64_t stride1,
+               uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle, CUtensorMap* map) {
+  struct Entry {
+    const void* base;
+    uint64_t dim0, dim1, stride1;
+    uint32_t box0, box1;
+    int type, swizzle;
+    bool valid;
+    CUtensorMap map;
+  };
+  constexpr int kEntries = 16;
+  thread_local Entry cache[kEntries] = {};
+  thread_local int next = 0;
+  for (int i = 0; i < kEntries; ++i) {
+    const Entry& e = cache[i];
+    if (e.valid && e.base == base && e.dim0 == dim0 && e.dim1 == dim1 && e.stride1 == stride1 && e.box0 == box0 &&
+        e.box1 == box1 && e.type == static_cast<int>(type) && e.swizzle == static_cast<int>(swizzle)) {
+      *map = e.map;
+      return true;
+    }
+  }
+  auto encode = tensor_map_encoder();
+  if (encode == nullptr) return false;
+  cuuint64_t dims[2] = {dim0, dim1};
+  cuuint64_t strides[1] = {stride1};
+  cuuint32_t box[2] = {box0, box1};
+  cuuint32_t elem_strides[2] = {1, 1};
+  if (encode(map, type, 2, const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  Entry& e = cache[next];
+  next = (next + 1) % kEntries;
+  e = Entry{base, dim0, dim1, stride1, box0, box1, static_cast<int>(type), static_cast<int>(swizzle), true, *map};
+  return true;
+}
+
 // 2-D map over the packed weight codes [n_pad, K/2] bytes: 128 x 128-byte
 // boxes, 128-byte swizzle (the canonical K-major layout the MMA descriptor
 // reads); columns past K/2 read as zero.
 bool encode_weight_map(const void* bpacked, int64_t N, int64_t K, CUtensorMap* map) {
-  auto encode = tensor_map_encoder();
-  if (encode == nullptr) return false;
   const PackedLayout L = packed_layout(N, K);
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(L.n_pad)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKBytes), static_cast<cuuint32_t>(kTileN)};
-  cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(bpacked), dims, strides,
-                            box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_2d(CU_TENSOR_MAP_DATA_TYPE_UINT8, bpacked, static_cast<uint64_t>(K / 2),
+                   static_cast<uint64_t>(L.n_pad), static_cast<uint64_t>(K / 2), kTileKBytes, kTileN,
+                   CU_TENSOR_MAP_SWIZZLE_128B, map);
 }
 
 // 2-D map over the activation for one GEMM launch: bf16 [M, lda] with
@@ -113,27 +147,12 @@ int activation_box_rows(int64_t M, int block_m) {
 
 bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, bool fused, int block_m,
                            CUtensorMap* map) {
-  const int rows = activation_box_rows(M, block_m);
-  auto encode = tensor_map_encoder();
-  if (encode == nullptr) return false;
-  cuuint32_t elem_strides[2] = {1, 1};
-  CUresult r;
-  if (fused) {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(lda * 2)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileK), static_cast<cuuint32_t>(rows)};
-    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(a), dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  } else {
-    cuuint64_t dims[2] = {static_cast<cuuint64_t>(K / 2), static_cast<cuuint64_t>(M)};
-    cuuint64_t strides[1] = {static_cast<cuuint64_t>(K / 2)};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileKBytes), static_cast<cuuint32_t>(rows)};
-    r = encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(a), dims, strides, box, elem_strides,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  }
-  return r == CUDA_SUCCESS;
+  const uint32_t rows = static_cast<uint32_t>(activation_box_rows(M, block_m));
+  if (fused)
+    return encode_2d(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, a, static_cast<uint64_t>(K), static_cast<uint64_t>(M),
+                     static_cast<uint64_t>(lda * 2), kTileK, rows, CU_TENSOR_MAP_SWIZZLE_NONE, map);
+  return encode_2d(CU_TENSOR_MAP_DATA_TYPE_UINT8, a, static_cast<uint64_t>(K / 2), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(K / 2), kTileKBytes, rows, CU_TENSOR_MAP_SWIZZLE_128B, map);
 }
 
 // 2-D map over the output C [M, N] bf16 for the TMA store of a whole
@@ -141,16 +160,9 @@ bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, boo
 // written).  Needs N * 2 bytes per row to be a multiple of 16.
 bool encode_output_map(void* c, int64_t M, int64_t N, int block_m, CUtensorMap* map) {
   if (N % 8 != 0) return false;
-  auto encode = tensor_map_encoder();
-  if (encode == nullptr) return false;
-  cuuint64_t dims[2] = {static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(M)};
-  cuuint64_t strides[1] = {static_cast<cuuint64_t>(N * 2)};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kTileN), static_cast<cuuint32_t>(block_m)};
-  cuuint32_t elem_strides[2] = {1, 1};
-  const CUresult r = encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, c, dims, strides, box, elem_strides,
-                            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
+  return encode_2d(CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, c, static_cast<uint64_t>(N), static_cast<uint64_t>(M),
+                   static_cast<uint64_t>(N * 2), kTileN, static_cast<uint32_t>(block_m), CU_TENSOR_MAP_SWIZZLE_NONE,
+                   map);
 }
 
 // The default plan per (device, M, N, K, fused), computed once: the plan
