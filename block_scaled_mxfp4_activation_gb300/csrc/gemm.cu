@@ -22,14 +22,16 @@
 //   - warp 1 moves both scale sets to tensor memory (tcgen05.cp) and issues
 //     four K = 64 block-scaled MMAs per stage into an fp32 accumulator in
 //     tensor memory;
+//   - without a K split, the accumulator leaves as bf16 through a tile in
+//     shared memory and one TMA tensor store;
 //   - K splits of one output tile form a thread-block cluster: each CTA
-//     stages its fp32 partial tile in shared memory and the cluster sums the
-//     partials through distributed shared memory in a fixed order
-//     (deterministic, no global workspace, no second kernel);
-//   - bf16 is written with 8-byte coalesced stores.
+//     pushes its fp32 partial blocks to their owners' shared memory and every
+//     owner sums its blocks over the splits in a fixed order (deterministic,
+//     no global workspace, no second kernel), then stores 8 bytes per thread.
 //
 // Back-to-back calls overlap through programmatic dependent launch: the next
-// call's CTAs set up and prefetch their operands into L2 while this one ends.
+// call's CTAs set up and load their weights into shared memory while this one
+// runs (at most one call ahead).
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
