@@ -276,9 +276,51 @@ def cpu_baseline(name: str, budget_s: float = 12.0) -> dict:
         n_sample = min(n_sample * 2, 1 << 16)
     per_elem = spent / done
     us = (t_quant + per_elem * w.M * w.N) * 1e6
-    return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "elements": done,
             "sample": f"{name}: one full A quantization + {done} randomly sampled output elements "
                       f"(of {w.M * w.N} per call; fp64, ascending k) in {spent:.1f} s, scaled to M*N"}
+
+
+def _oracle_sampled_chunk(args) -> float:
+    """Worker of cpu_baseline_all_cores: the oracle's sampled sum over one chunk
+    of output elements (a separate process with its own copy of the oracle)."""
+    aq, as_, bq, bs, ms, ns = args
+    import oracle
+
+    t0 = time.perf_counter()
+    oracle.gemm_sampled(aq, as_, bq, bs, ms, ns)
+    return time.perf_counter() - t0
+
+
+def cpu_baseline_all_cores(name: str, per_core_elems: int, cores: int | None = None) -> dict:
+    """The same oracle on every host core: one process per core (spawned, so
+    none inherits the parent's CUDA state), each summing its own chunk of
+    randomly sampled output elements; wall time scaled to M*N (plus the one
+    activation quantization, which stays on one core)."""
+    import multiprocessing as mp
+
+    import oracle
+
+    cores = cores or os.cpu_count() or 1
+    w = workloads.WORKLOADS[name]
+    A, B = workloads.make_inputs(w)
+    bq, bs = oracle.quantize(B)
+    t0 = time.perf_counter()
+    aq, as_ = oracle.quantize(A)
+    t_quant = time.perf_counter() - t0
+    rng = np.random.default_rng(1)
+    chunks = [(aq, as_, bq, bs, rng.integers(0, w.M, per_core_elems), rng.integers(0, w.N, per_core_elems))
+              for _ in range(cores)]
+    with mp.get_context("spawn").Pool(cores) as pool:
+        pool.map(_oracle_sampled_chunk, [(aq, as_, bq, bs, c[4][:16], c[5][:16]) for c in chunks])  # start-up
+        t0 = time.perf_counter()
+        pool.map(_oracle_sampled_chunk, chunks, chunksize=1)
+        wall = time.perf_counter() - t0
+    done = per_core_elems * cores
+    us = (t_quant + wall * w.M * w.N / done) * 1e6
+    return {"value": round(us, 1), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{name}: one full A quantization + {done} randomly sampled output elements in {cores} "
+                      f"processes ({wall:.1f} s wall), scaled to M*N"}
 
 
 def run_ours(args) -> dict:
@@ -365,6 +407,9 @@ def run_ours(args) -> dict:
         out["per_shape"] = shapes
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(name)
+        # all host cores, each process on half as many elements as the one-core run summed
+        per_core = max(256, out["cpu_baseline"]["elements"] // 2)
+        out["cpu_baseline_all_cores"] = cpu_baseline_all_cores(name, per_core)
     if world > 1:
         import torch.distributed as dist
 
