@@ -140,10 +140,6 @@ bool encode_weight_map(const void* bpacked, int64_t N, int64_t K, CUtensorMap* m
 // memory), or codes [M, K/2] with 128-byte x block_m boxes and the 128-byte
 // swizzle (landing directly in the MMA operand layout).  Rows past M and
 // columns past K read as zero.
-int activation_box_rows(int64_t M, int block_m) {
-  const int64_t r = (M + 7) / 8 * 8;
-  return static_cast<int>(r < block_m ? r : block_m);
-}
 
 bool encode_activation_map(const void* a, int64_t M, int64_t K, int64_t lda, bool fused, int block_m,
                            CUtensorMap* map) {
@@ -262,6 +258,7 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   const GemmLayout GL = gemm_layout(plan.block_m, plan.stages, plan.splits, fused, M);
   g.a_off = GL.a_off;
   g.abf_off = GL.abf_off;
+  g.abf_stage_bytes = GL.abf_stage;
   g.sfw_off = GL.sfw_off;
   g.sfa_off = GL.sfa_off;
   g.stg_off = GL.stg_off;

@@ -43,7 +43,6 @@ struct TileCfg {
   static constexpr int kRowChunks = BM > 128 ? 2 : 1;             // 128-row scale chunks of A
   static constexpr int kBTileBytes = kTileN * kTileKBytes;         // 16 KB of weight codes
   static constexpr int kATileBytes = BM * kTileKBytes;             // activation codes
-  static constexpr int kAbfBytes = kFused ? BM * kTileK * 2 : 0;   // bf16 activation staging
   static constexpr int kSfaStageBytes = 2 * kRowChunks * kSfChunkBytes;
   static constexpr int kAWarps = 8;                                // producer / epilogue warps
   static constexpr int kAThreads = kAWarps * 32;
@@ -212,7 +211,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       const int s = i % stages, kt = kt_begin + i;
       const uint32_t bar = full_in(s);
       if constexpr (kFused) {
-        const uint32_t dst = sbase + args.abf_off + s * C::kAbfBytes;
+        const uint32_t dst = sbase + args.abf_off + s * args.abf_stage_bytes;
         if (leader) {
           mbar_arrive_expect_tx(bar, args.a_box_rows * kTileK * 2);
           tma_load_2d(dst, &tmap_a, kt * kTileK, m_base, bar, policy_a);
@@ -378,7 +377,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       uint8_t* a_tile = smem + args.a_off + s * C::kATileBytes;
       uint8_t* sfa = smem + args.sfa_off + s * C::kSfaStageBytes;
       if constexpr (kFused) {
-        const uint8_t* abf = smem + args.abf_off + s * C::kAbfBytes;
+        const uint8_t* abf = smem + args.abf_off + s * args.abf_stage_bytes;
         if (m_valid >= BM)
           quantize_tile<BM, C::kAThreads, C::kRowChunks, false>(abf, a_tile, sfa, tid, m_valid);
         else
@@ -599,7 +598,8 @@ GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t 
   const uint32_t st = static_cast<uint32_t>(stages), bm = static_cast<uint32_t>(block_m);
   L.a_off = st * kTileN * kTileKBytes;
   L.abf_off = L.a_off + st * bm * kTileKBytes;
-  L.sfw_off = L.abf_off + (fused ? st * bm * kTileK * 2 : 0u);
+  L.abf_stage = fused ? static_cast<uint32_t>(activation_box_rows(M, block_m)) * kTileK * 2 : 0u;
+  L.sfw_off = L.abf_off + st * L.abf_stage;
   // without a K split the bf16 output tile is written over the operand
   // buffers once the MMAs are done: keep room for it before the scales
   if (splits == 1 && L.sfw_off < bm * kTileN * 2) L.sfw_off = bm * kTileN * 2;
@@ -703,10 +703,9 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // that overlap costs more than any stage depth gains (K = 7168, 7 splits: 2
 // stages 5.6 us, 4 stages with one CTA per SM 10.0 us).  Candidates: block_m
 // from the smallest tile that holds M (capped at 256) down to a quarter of it;
-// every split count that leaves no split empty; one or two stages, or every K
-// tile of the split when that still fits.  Ties prefer the larger block_m
-// (fewer re-reads of the weights), then the larger stage count, then fewer
-// splits.
+// every split count that leaves no split empty; 1 to 6 stages (at most the
+// split's K tiles).  Ties prefer the larger block_m (fewer re-reads of the
+// weights), then the larger stage count, then fewer splits.
 // Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
 // the estimate is not: sweeps of block_m x splits x stages, graph-replayed
 // calls with rotating operands.  `fused` is the GEMM kernel's kind (the large-M
@@ -717,7 +716,7 @@ struct TunedPlan {
   int block_m, splits, stages;
 };
 constexpr TunedPlan kTunedPlans[] = {
-    {16, 2112, 7168, true, 32, 7, 2},
+    {16, 2112, 7168, true, 32, 7, 3},
     {64, 7168, 2048, false, 64, 4, 2},
     {256, 3072, 1536, false, 64, 2, 3},
 };
@@ -753,8 +752,7 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
     for (int64_t splits = 1; splits <= kMaxSplits && splits <= k_tiles; ++splits) {
       const int64_t per = ceil_div(k_tiles, splits);
       if ((splits - 1) * per >= k_tiles) continue;  // an empty split
-      for (int64_t st : {int64_t(1), int64_t(2), per}) {
-        if (st > per || st > 6 || (st == per && per <= 2 && st != 1 && st != 2)) continue;
+      for (int64_t st = 1; st <= per && st <= 6; ++st) {
         mxfp4_plan_t q{};
         q.block_m = bm;
         q.splits = static_cast<int32_t>(splits);

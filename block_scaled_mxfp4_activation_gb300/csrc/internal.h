@@ -61,20 +61,30 @@ struct GemmArgs {
   uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off;
   int32_t stg_blocks;       // 32 x 16 partial blocks each CTA may receive from one split
   int32_t a_box_rows;       // rows of one activation TMA box: min(block_m, roundup(M, 8))
+  uint32_t abf_stage_bytes; // fused: bf16 staging per stage, a_box_rows x 512 bytes
   int32_t accumulators;     // independent fp32 accumulator tiles in tensor memory (1, 2, 4)
   int32_t c_tma;            // no K split: C leaves through a bf16 tile in shared memory and one TMA store
   int32_t trigger_late;     // let the next grid launch only once this grid has passed its own wait
 };
 
 // Shared-memory layout of one GEMM CTA (byte offsets from a 1024-aligned base):
-// weight code tiles, activation code tiles, bf16 activation staging (fused),
+// weight code tiles, activation code tiles, bf16 activation staging (fused,
+// activation_box_rows x 512 bytes per stage),
 // weight scales, activation scales (one of each per stage), the split-K
 // staging slots ([splits][stg_blocks] blocks of 2 KB), then the mbarriers.
 // Without a K split the bf16 output tile [block_m][128] is staged at offset 0
 // once the MMAs are done (the operand buffers are free by then); the layout
 // keeps at least block_m x 256 bytes before the scales for it.
+// Rows of one activation TMA box (and of the bf16 staging): the tile's rows
+// that can hold data, rounded up to 8.
+inline int activation_box_rows(int64_t M, int block_m) {
+  const int64_t r = (M + 7) / 8 * 8;
+  return static_cast<int>(r < block_m ? r : block_m);
+}
+
 struct GemmLayout {
   uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off, total;
+  uint32_t abf_stage;  // bf16 staging bytes per stage (fused)
   int32_t stg_blocks;
 };
 GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M);
