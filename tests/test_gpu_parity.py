@@ -198,6 +198,32 @@ def test_fused_quantization_bitexact_through_identity(oracle_mod, M):
         assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} differ, first at {np.argwhere(bad)[0]}"
 
 
+def random_shapes(n: int, seed: int):
+    """Seeded (M, N, K) with tails in every dimension: M 1..96, N 1..400,
+    K a multiple of 32 up to 1536 (K % 256 and K % 64 both vary)."""
+    rng = np.random.default_rng(seed)
+    return [(int(rng.integers(1, 97)), int(rng.integers(1, 401)), 32 * int(rng.integers(1, 49))) for _ in range(n)]
+
+
+@pytest.mark.parametrize("M,N,K", random_shapes(24, seed=2024))
+def test_gemm_random_shapes(oracle_mod, M, N, K):
+    """Random ragged shapes through every route (the default plan, the single
+    fused kernel, the unfused GEMM on the standalone quantizer's codes) against
+    the oracle; the codes and scales bit-exact."""
+    A, B = workloads.make_random(M, N, K, seed=M * 131 + N * 7 + K)
+    bq, bs, W = quantized_weight(oracle_mod, B)
+    aq, as_, c64, _ = oracle_mod.quant_gemm(A, bq, bs)
+    Ad = A.cuda()
+    Aq, As = mx.quantize(Ad)
+    C_default = mx.quant_gemm(Ad, W)
+    C_single = mx.quant_gemm(Ad, W, workspace=torch.empty(0, dtype=torch.uint8, device="cuda"))
+    C_unfused = mx.gemm(Aq, As, W)
+    torch.cuda.synchronize()
+    assert np.array_equal(Aq.cpu().numpy(), aq) and np.array_equal(As.cpu().numpy(), as_)
+    for what, C in (("default", C_default), ("single fused kernel", C_single), ("unfused", C_unfused)):
+        check_close(C, c64, f"{what} {M}x{N}x{K}")
+
+
 def test_gemm_every_plan_agrees(oracle_mod):
     M, N, K = 40, 384, 2048
     A, B = workloads.make_random(M, N, K, seed=99)
