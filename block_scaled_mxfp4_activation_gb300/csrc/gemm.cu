@@ -440,11 +440,16 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       }
       if (splits == 1 && args.c_tma) {
         // no K split: bf16 into the output tile [BM rows][128 columns] at
-        // offset 0 (lane = column n, register e = row m; a warp's stores of
-        // one row are 64 contiguous bytes), sent by one TMA store below
+        // offset 0 (lane = column n, register e = row m, rows e and e + 1
+        // converted as one pair; a warp's stores of one row are 64 contiguous
+        // bytes), sent by one TMA store below
         __nv_bfloat16* cs = reinterpret_cast<__nv_bfloat16*>(smem) + (c * 16) * kTileN + qr * 32 + lane;
 #pragma unroll
-        for (int e = 0; e < 16; ++e) cs[e * kTileN] = __float2bfloat16_rn(__uint_as_float(r[e]));
+        for (int e = 0; e < 16; e += 2) {
+          const __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(r[e]), __uint_as_float(r[e + 1]));
+          cs[e * kTileN] = pr.x;
+          cs[(e + 1) * kTileN] = pr.y;
+        }
         continue;
       }
       if (splits == 1) {
