@@ -48,7 +48,7 @@ struct TileCfg {
   static constexpr int kAThreads = kAWarps * 32;
   static constexpr int kThreads = 64 + kAThreads;
   static constexpr int kSfCols = 8 + 8 * kRowChunks;               // TMEM scale columns per stage
-  static_assert(BM % 32 == 0 && BM <= 256, "block_m must be 32, 64, 128 or 256");
+  static_assert(BM == 16 || BM == 32 || BM == 64 || BM == 128 || BM == 256, "block_m must be 16, 32, 64, 128 or 256");
 };
 
 // The accumulator tile (128 weight rows x BM activation rows) is reduced over
@@ -579,6 +579,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, co
     return fused ? launch_t<BM_, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s)     \
                  : launch_t<BM_, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);
   switch (plan.block_m) {
+    MXFP4_LAUNCH(16)
     MXFP4_LAUNCH(32)
     MXFP4_LAUNCH(64)
     MXFP4_LAUNCH(128)
@@ -620,7 +621,8 @@ GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t 
 
 bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                  mxfp4_plan_t* p) {
-  if (p->block_m != 32 && p->block_m != 64 && p->block_m != 128 && p->block_m != 256) return false;
+  if (p->block_m != 16 && p->block_m != 32 && p->block_m != 64 && p->block_m != 128 && p->block_m != 256)
+    return false;
   const int64_t k_tiles = ceil_div(K, kTileK);
   if (p->splits < 1 || p->splits > kMaxSplits || p->splits > k_tiles) return false;
   const int64_t per = ceil_div(k_tiles, p->splits);
@@ -687,6 +689,7 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 #define MXFP4_OCC(BM_) \
   case BM_: return fused ? active_clusters_t<BM_, true>(p) : active_clusters_t<BM_, false>(p);
   switch (p.block_m) {
+    MXFP4_OCC(16)
     MXFP4_OCC(32)
     MXFP4_OCC(64)
     MXFP4_OCC(128)
@@ -701,7 +704,8 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // wave (every cluster resident at once, at most two CTAs per SM): each K tile
 // a split runs in sequence costs ~250 ns (operand loads, tensor-memory scale
 // copies, four MMAs) plus, on the fused kernel, ~200 ns per 32 activation rows
-// it quantizes; a K split adds ~700 ns for the cluster reduction (measured on
+// it quantizes (so 16-row tiles halve it: at M = 32 two CTAs of 16 rows beat
+// one of 32); a K split adds ~700 ns for the cluster reduction (measured on
 // GB300 with graph-replayed calls).  Among plans that run in one wave, those
 // whose shared memory lets two CTAs share an SM come first: the next call's
 // CTAs then start early beside this call's (programmatic launch), and losing
@@ -721,7 +725,7 @@ struct TunedPlan {
   int block_m, splits, stages;
 };
 constexpr TunedPlan kTunedPlans[] = {
-    {16, 2112, 7168, true, 32, 7, 3},
+    {16, 2112, 7168, true, 16, 7, 3},
     {64, 7168, 2048, false, 64, 4, 2},
     {256, 3072, 1536, false, 64, 2, 3},
 };
@@ -729,7 +733,7 @@ constexpr TunedPlan kTunedPlans[] = {
 // Estimated critical path of one CTA, in ns (see above).
 static int64_t plan_cost_ns(const mxfp4_plan_t& p, int64_t M, bool fused) {
   const int64_t rows = M < p.block_m ? M : p.block_m;
-  const int64_t tile = 250 + (fused ? 200 * ceil_div(rows, 32) : 0);
+  const int64_t tile = 250 + (fused ? 200 * rows / 32 : 0);
   return p.k_tiles_per_split * tile + (p.splits > 1 ? 700 : 0);
 }
 
@@ -749,11 +753,11 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
       }
     }
   }
-  const int bm0 = M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  const int bm0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
   const int64_t k_tiles = ceil_div(K, kTileK);
   const int64_t cap = 2 * static_cast<int64_t>(prop.multiProcessorCount);
   int64_t best[6] = {-1, 0, 0, 0, 0, 0};
-  for (int bm = bm0; bm >= 32 && bm * 4 >= bm0; bm /= 2) {
+  for (int bm = bm0; bm >= 16 && bm * 4 >= bm0; bm /= 2) {
     for (int64_t splits = 1; splits <= kMaxSplits && splits <= k_tiles; ++splits) {
       const int64_t per = ceil_div(k_tiles, splits);
       if ((splits - 1) * per >= k_tiles) continue;  // an empty split

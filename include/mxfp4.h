@@ -53,7 +53,7 @@ typedef enum {
 
 /* Tile plan of one GEMM launch (see mxfp4_gemm_plan). */
 typedef struct {
-  int32_t block_m;    /* activation rows per CTA = the MMA's N: 32, 64, 128 or 256 */
+  int32_t block_m;    /* activation rows per CTA = the MMA's N: 16, 32, 64, 128 or 256 */
   int32_t splits;     /* K splits per output tile = CTAs per thread-block cluster, 1..8 */
   int32_t stages;     /* shared-memory pipeline depth in K tiles of 256 */
   int32_t k_tiles_per_split;

@@ -181,14 +181,14 @@ def test_fused_quantization_bitexact_through_identity(oracle_mod, M):
     assert np.array_equal(expect.astype(np.float32).astype(np.float64), expect)
     Ad = A.cuda()
     results = {"single fused kernel": mx.quant_gemm(Ad, W, workspace=torch.empty(0, dtype=torch.uint8, device="cuda"))}
-    for bm in (32, 64, 128, 256):
+    for bm in (16, 32, 64, 128, 256):
         for splits in (1, 2):
             plan = {"block_m": bm, "splits": splits, "stages": 1}
             try:
                 results[f"fused plan {plan}"] = mx.gemm_with_plan(Ad, None, W, plan, True)
             except mx.MXFP4Error as e:
                 assert e.status == 1 and bm == 256, plan  # only a 256-row tile may not fit in shared memory
-    assert len(results) >= 8
+    assert len(results) >= 10
     Aq, As = mx.quantize(Ad)
     results["quantize + unfused"] = mx.gemm(Aq, As, W)
     torch.cuda.synchronize()
@@ -232,7 +232,7 @@ def test_gemm_every_plan_agrees(oracle_mod):
     Ad = A.cuda()
     Aq, As = mx.quantize(Ad)
     ran, rejected = [], []
-    for bm in (32, 64, 128, 256):
+    for bm in (16, 32, 64, 128, 256):
         for splits in (1, 2, 4, 8):
             for stages in (1, 2, 3):
                 plan = {"block_m": bm, "splits": splits, "stages": stages}
@@ -247,9 +247,9 @@ def test_gemm_every_plan_agrees(oracle_mod):
                     check_close(C, c64, f"plan {plan} fused={fused}")
                     ran.append((bm, splits, stages, fused))
     # every (block_m, splits, path) ran with at least one stage count
-    assert {(b, s, f) for b, s, _, f in ran} == {(b, s, f) for b in (32, 64, 128, 256) for s in (1, 2, 4, 8)
+    assert {(b, s, f) for b, s, _, f in ran} == {(b, s, f) for b in (16, 32, 64, 128, 256) for s in (1, 2, 4, 8)
                                                  for f in (True, False)}
-    assert len(ran) >= 80, rejected
+    assert len(ran) >= 100, rejected
 
 
 @pytest.mark.parametrize("accumulators", [1, 2, 4])
