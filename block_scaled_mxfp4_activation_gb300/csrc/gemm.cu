@@ -271,27 +271,39 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     // lane's earlier operations.
     const bool leader = elect_one();
     bool triggered = !args.trigger_late;
-    for (int i = 0; i < kt_count; ++i) {
-      const int s = i % stages, round = i / stages;
-      const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
-      const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
-      const uint32_t sfw_s = sbase + args.sfw_off + s * kSfTileBytes;
-      const uint32_t sfa_s = sbase + args.sfa_off + s * C::kSfaStageBytes;
-      const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
-      const uint64_t b_desc = smem_desc(sbase + args.a_off + s * C::kATileBytes, 16, 1024, 2);
-      const int k0 = (kt_begin + i) * kTileK;
+    // Weight scales of stage s to tensor memory once the stage's weights have
+    // landed; false if the wait gave up.
+    auto weight_scales = [&](int s, int round) {
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_w(s), round & 1, timeout))) {
         if (leader) report_error(args.err, kErrWaitTma);
         *abort_flag = 1u;
       }
-      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) return false;
       tc_fence_after_sync();
-      // the weight scales can move to tensor memory while the activation is still being prepared
+      const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
+      const uint32_t sfw_s = sbase + args.sfw_off + s * kSfTileBytes;
       if (leader) {
 #pragma unroll
         for (int c = 0; c < 2; ++c) tmem_cp_32x128b_warpx4(sfw_t + 4 * c, smem_desc(sfw_s + c * kSfChunkBytes, 128, 128, 0));
       }
       __syncwarp();
+      return true;
+    };
+    // The stages loaded first hold weights that arrive before the activation
+    // (under programmatic launch, before the previous grid has finished): their
+    // scales go to tensor memory up front, off the activation's critical path.
+    const int pre = min(stages, kt_count);
+    bool alive = true;
+    for (int i = 0; i < pre && alive; ++i) alive = weight_scales(i, 0);
+    for (int i = 0; i < kt_count && alive; ++i) {
+      const int s = i % stages, round = i / stages;
+      const uint32_t sfw_t = tmem_sf + s * C::kSfCols;
+      const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
+      const uint32_t sfa_s = sbase + args.sfa_off + s * C::kSfaStageBytes;
+      const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
+      const uint64_t b_desc = smem_desc(sbase + args.a_off + s * C::kATileBytes, 16, 1024, 2);
+      const int k0 = (kt_begin + i) * kTileK;
+      if (i >= stages && !weight_scales(s, round)) break;  // a reloaded stage
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_a(s), round & 1, timeout))) {
         if (leader) report_error(args.err, kErrWaitA);
         *abort_flag = 1u;
