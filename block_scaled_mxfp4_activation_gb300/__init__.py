@@ -273,7 +273,8 @@ def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
 def quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, C_dev: torch.Tensor,
                     C_host: torch.Tensor, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """The fused layer on host data in one call: A_host (pinned CPU bf16 [M, K]) -> A_dev ->
-    quantize + GEMM -> C_dev -> C_host (pinned CPU bf16 [M, N]); asynchronous on the stream."""
+    quantize + GEMM -> C_dev and C_host (pinned CPU bf16 [M, N], written by the GEMM kernel
+    itself when the device can address it); asynchronous on the stream."""
     W = _weight(W)
     for t, dev, what in ((A_host, False, "A_host"), (C_host, False, "C_host"), (A_dev, True, "A_dev"),
                          (C_dev, True, "C_dev")):

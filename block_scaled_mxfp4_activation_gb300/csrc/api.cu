@@ -207,9 +207,11 @@ mxfp4_status_t check_mnk(int64_t M, int64_t N, int64_t K) {
   return MXFP4_OK;
 }
 
+// c_host: null, or the device address of a second [M, N] output in mapped
+// host memory that the kernel writes alongside C.
 mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* bpacked, void* C,
                         int64_t M, int64_t N, int64_t K, bool fused, const mxfp4_plan_t* user_plan,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, void* c_host = nullptr) {
   mxfp4_status_t st = check_mnk(M, N, K);
   if (st != MXFP4_OK) return st;
   if (a == nullptr || bpacked == nullptr || C == nullptr || (!fused && as == nullptr))
@@ -245,6 +247,7 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   const PackedLayout L = packed_layout(N, K);
   g.b_sf = static_cast<const uint8_t*>(bpacked) + L.sf_offset;
   g.c = static_cast<__nv_bfloat16*>(C);
+  g.c_host = static_cast<__nv_bfloat16*>(c_host);
   g.M = static_cast<int32_t>(M);
   g.N = static_cast<int32_t>(N);
   g.K = static_cast<int32_t>(K);
@@ -275,6 +278,28 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("GEMM launch", e);
 }
 
+// mxfp4_quant_gemm, with the optional host copy of C (see run_gemm).
+mxfp4_status_t quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M, int64_t N,
+                          int64_t K, void* ws, size_t ws_bytes, cudaStream_t s, void* c_host) {
+  mxfp4_status_t st = check_mnk(M, N, K);
+  if (st != MXFP4_OK) return st;
+  if (two_pass_wanted(M) && ws != nullptr && ws_bytes >= two_pass_workspace(M, K) && aligned16(ws)) {
+    // validate everything the GEMM checks before anything is launched
+    if (A == nullptr || Bpacked == nullptr || C == nullptr) return MXFP4_ERR_INVALID_ARG;
+    if (lda < K) return MXFP4_ERR_INVALID_ARG;
+    if (!aligned16(A) || !aligned16(Bpacked) || !aligned16(C) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
+    if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+    // Two passes: quantize A once into the workspace, then the GEMM on codes
+    // (the fused kernel would re-read the 4x larger bf16 A in every N tile).
+    uint8_t* Aq = static_cast<uint8_t*>(ws);
+    uint8_t* As = Aq + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
+    st = mxfp4_quantize(A, M, K, lda, Aq, As, s);
+    if (st != MXFP4_OK) return st;
+    return run_gemm(Aq, K / 2, As, Bpacked, C, M, N, K, false, nullptr, s, c_host);
+  }
+  return run_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, s, c_host);
+}
+
 }  // namespace
 
 void set_last_error(const char* what) { snprintf(g_last_error, sizeof(g_last_error), "%s", what); }
@@ -289,7 +314,7 @@ mxfp4_status_t mxfp4_quantize(const void* A, int64_t M, int64_t K, int64_t lda, 
                               mxfp4_stream_t stream) {
   if (A == nullptr || Aq == nullptr || As == nullptr) return MXFP4_ERR_INVALID_ARG;
   if (M < 1 || K < 32 || K % 32 != 0 || lda < K) return MXFP4_ERR_INVALID_ARG;
-  if (M > kMaxDim || K > kMaxDim || M * (K / 8) > (int64_t(1) << 31) * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (M > kMaxDim || K > kMaxDim || M * (K / 16) > (int64_t(1) << 31) * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   if (!aligned16(A) || !aligned16(Aq) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
   mxfp4_status_t st;
   if (current_device(&st) == nullptr) return st;
@@ -354,24 +379,7 @@ mxfp4_status_t mxfp4_gemm(const void* Aq, const void* As, const void* Bpacked, v
 
 mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  mxfp4_status_t st = check_mnk(M, N, K);
-  if (st != MXFP4_OK) return st;
-  if (two_pass_wanted(M) && ws != nullptr && ws_bytes >= two_pass_workspace(M, K) && aligned16(ws)) {
-    // validate everything the GEMM checks before anything is launched
-    if (A == nullptr || Bpacked == nullptr || C == nullptr) return MXFP4_ERR_INVALID_ARG;
-    if (lda < K) return MXFP4_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(Bpacked) || !aligned16(C) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
-    if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-    // Two passes: quantize A once into the workspace, then the GEMM on codes
-    // (the fused kernel would re-read the 4x larger bf16 A in every N tile).
-    uint8_t* Aq = static_cast<uint8_t*>(ws);
-    uint8_t* As = Aq + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
-    st = mxfp4_quantize(A, M, K, lda, Aq, As, stream);
-    if (st != MXFP4_OK) return st;
-    return run_gemm(Aq, K / 2, As, Bpacked, C, M, N, K, false, nullptr, s);
-  }
-  return run_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, s);
+  return quant_gemm(A, lda, Bpacked, C, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
 }
 
 mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void* A_dev, int64_t lda_dev,
@@ -402,14 +410,13 @@ mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void*
                           static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
   }
   if (e != cudaSuccess) return cuda_failure("activation upload", e);
-  st = mxfp4_quant_gemm(A_dev, lda_dev, Bpacked, C_dev, M, N, K, ws, ws_bytes, stream);
-  if (st != MXFP4_OK) return st;
-  const int64_t c_bytes = M * N * 2;
+  // A mapped C_host is written by the GEMM kernel itself, beside C_dev (no
+  // download pass); any other by the copy engines afterwards.
   void* c_dst = const_cast<void*>(device_view(C_host));
-  if (c_dst != nullptr && aligned16(c_dst) && c_bytes % 16 == 0)
-    e = launch_copy_rows(C_dev, c_bytes, c_dst, c_bytes, c_bytes, 1, false, programmatic, sms, s);
-  else
-    e = cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(c_bytes), cudaMemcpyDeviceToHost, s);
+  const bool c_direct = c_dst != nullptr && aligned16(c_dst);
+  st = quant_gemm(A_dev, lda_dev, Bpacked, C_dev, M, N, K, ws, ws_bytes, s, c_direct ? c_dst : nullptr);
+  if (st != MXFP4_OK || c_direct) return st;
+  e = cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(M * N * 2), cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("result download", e);
 }
 

@@ -122,7 +122,9 @@ __device__ __forceinline__ void quantize_tile(const uint8_t* abf, uint8_t* a_til
   }
 }
 
-template <int BM, bool kFused>
+// kHostC: every element of C is also written to args.c_host (mapped host
+// memory); a separate instantiation, so the common kernels carry none of it.
+template <int BM, bool kFused, bool kHostC>
 __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
@@ -350,7 +352,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       const int64_t j0 = static_cast<int64_t>(kt_begin + i) * 8;
       const uint8_t* src = args.a_scales + static_cast<int64_t>(m_base + tid) * nblk + j0;
       if (scales_vec8) {
-        const uint2 v = __ldg(reinterpret_cast<const uint2*>(src));
+        const uint2 v = ld_after_wait_v2(src);  // written by the quantize pass before this grid
         w0 = v.x;
         w1 = v.y;
         return;
@@ -358,7 +360,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       uint32_t w[2] = {0u, 0u};
 #pragma unroll
       for (int jb = 0; jb < 8; ++jb)
-        if (j0 + jb < nblk) w[jb >> 2] |= static_cast<uint32_t>(__ldg(src + jb)) << (8 * (jb & 3));
+        if (j0 + jb < nblk) w[jb >> 2] |= ld_after_wait_u8(src + jb) << (8 * (jb & 3));
       w0 = w[0];
       w1 = w[1];
     };
@@ -473,6 +475,12 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
 #pragma unroll
           for (int e = 0; e < 16; ++e)
             if (c * 16 + e < m_valid) col[static_cast<int64_t>(c * 16 + e) * args.N] = __float2bfloat16_rn(__uint_as_float(r[e]));
+          if constexpr (kHostC) {
+            __nv_bfloat16* hcol = args.c_host + static_cast<int64_t>(m_base) * args.N + n;
+#pragma unroll
+            for (int e = 0; e < 16; ++e)
+              if (c * 16 + e < m_valid) hcol[static_cast<int64_t>(c * 16 + e) * args.N] = __float2bfloat16_rn(__uint_as_float(r[e]));
+          }
         }
         continue;
       }
@@ -500,6 +508,18 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       if (tid == 0) {
         tma_store_2d(&tmap_c, n_tile * kTileN, m_base, sbase);
         bulk_commit_group();
+      }
+      if constexpr (kHostC) {
+        // the host copy of the tile, read back from shared memory 16 bytes at
+        // a time: row m, 8 columns per chunk (N % 8 == 0 here, so a chunk is
+        // wholly inside or wholly past N), 256 contiguous bytes per row
+        const int n_base = n_tile * kTileN;
+        for (int it = tid; it < m_valid * 16; it += C::kAThreads) {
+          const int m = it >> 4, n = n_base + (it & 15) * 8;
+          if (n < args.N)
+            *reinterpret_cast<uint4*>(args.c_host + static_cast<int64_t>(m_base + m) * args.N + n) =
+                *reinterpret_cast<const uint4*>(smem + (m * kTileN + (it & 15) * 8) * 2);
+        }
       }
     }
   }
@@ -541,10 +561,14 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         wv.x = *reinterpret_cast<const uint32_t*>(&lo);
         wv.y = *reinterpret_cast<const uint32_t*>(&hi);
         *reinterpret_cast<uint2*>(dst) = wv;
+        if constexpr (kHostC) *reinterpret_cast<uint2*>(args.c_host + gm * args.N + gn) = wv;
       } else {
         const float e[4] = {acc.x, acc.y, acc.z, acc.w};
         for (int qq = 0; qq < 4; ++qq)
-          if (gn + qq < args.N) dst[qq] = __float2bfloat16_rn(e[qq]);
+          if (gn + qq < args.N) {
+            dst[qq] = __float2bfloat16_rn(e[qq]);
+            if constexpr (kHostC) args.c_host[gm * args.N + gn + qq] = __float2bfloat16_rn(e[qq]);
+          }
       }
     }
   }
@@ -553,10 +577,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
 }
 
 // ----------------------------------------------------------------------------- host side
-template <int BM, bool kFused>
+template <int BM, bool kFused, bool kHostC>
 static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                             const GemmArgs& args, const mxfp4_plan_t& plan, bool programmatic, cudaStream_t s) {
-  auto kernel = mxfp4_gemm_kernel<BM, kFused>;
+  auto kernel = mxfp4_gemm_kernel<BM, kFused, kHostC>;
   static int configured_device = -1;  // max dynamic smem set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -586,10 +610,13 @@ static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a
 cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                         const GemmArgs& args, const mxfp4_plan_t& plan, bool fused, bool programmatic,
                         cudaStream_t s) {
-#define MXFP4_LAUNCH(BM_)                                                                       \
-  case BM_:                                                                                     \
-    return fused ? launch_t<BM_, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s)     \
-                 : launch_t<BM_, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);
+#define MXFP4_LAUNCH(BM_)                                                                           \
+  case BM_:                                                                                         \
+    if (args.c_host != nullptr)                                                                     \
+      return fused ? launch_t<BM_, true, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s) \
+                   : launch_t<BM_, false, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s); \
+    return fused ? launch_t<BM_, true, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s)  \
+                 : launch_t<BM_, false, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);
   switch (plan.block_m) {
     MXFP4_LAUNCH(16)
     MXFP4_LAUNCH(32)
@@ -675,7 +702,7 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
 
 template <int BM, bool kFused>
 static int active_clusters_t(const mxfp4_plan_t& p) {
-  auto kernel = mxfp4_gemm_kernel<BM, kFused>;
+  auto kernel = mxfp4_gemm_kernel<BM, kFused, false>;  // the host-copy kernels use the same resources
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid_x, p.grid_y, p.grid_z);
@@ -738,8 +765,8 @@ struct TunedPlan {
 };
 constexpr TunedPlan kTunedPlans[] = {
     {16, 2112, 7168, true, 16, 7, 3},
-    {64, 7168, 2048, false, 64, 4, 2},
-    {256, 3072, 1536, false, 64, 2, 3},
+    {64, 7168, 2048, false, 64, 2, 4},
+    {256, 3072, 1536, false, 64, 1, 6},
 };
 
 // Estimated critical path of one CTA, in ns (see above).

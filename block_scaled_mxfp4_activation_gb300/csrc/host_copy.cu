@@ -32,10 +32,9 @@ __global__ void __launch_bounds__(256) copy_rows_kernel(const uint8_t* __restric
     return;
   }
   grid_dependency_wait();
-  for (; i < total; i += stride) {
+  for (; i < total; i += stride) {  // the source may be the previous grid's output
     const int64_t r = i / per_row, c = i - r * per_row;
-    *reinterpret_cast<uint4*>(dst + r * dst_pitch + c * 16) =
-        *reinterpret_cast<const uint4*>(src + r * src_pitch + c * 16);
+    *reinterpret_cast<uint4*>(dst + r * dst_pitch + c * 16) = ld_after_wait_v4(src + r * src_pitch + c * 16);
   }
 }
 

@@ -47,6 +47,7 @@ struct GemmArgs {
   const uint8_t* a_scales;  // unfused: As [M, K/32]
   const uint8_t* b_sf;      // packed weight scales
   __nv_bfloat16* c;         // [M, N]
+  __nv_bfloat16* c_host;    // or null: a second copy of C, [M, N] in mapped host memory (device address)
   int32_t M, N, K;
   int64_t lda;              // fused: elements per row of A
   int32_t k_tiles;          // ceil(K / kTileK)

@@ -182,6 +182,32 @@ __device__ __forceinline__ void grid_dependency_wait() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Loads of data that an earlier grid on the stream may have written, for use
+// after grid_dependency_wait().  Inline asm keeps them after the wait (a load
+// through __ldg or a const __restrict__ pointer counts as invariant for the
+// kernel's lifetime and may be hoisted above it, reading the input before the
+// previous grid has written it), and .cg reads at L2, the point of coherence.
+__device__ __forceinline__ uint4 ld_after_wait_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.cg.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint2 ld_after_wait_v2(const void* p) {
+  uint2 v;
+  asm volatile("ld.global.cg.v2.u32 {%0, %1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ uint32_t ld_after_wait_u8(const void* p) {
+  uint32_t v;
+  asm volatile("ld.global.cg.u8 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // ----------------------------------------------------------------------------- tcgen05
 // Allocates `ncols` tensor-memory columns (a power of two >= 32); the whole
 // warp executes it and the address lands in shared memory at `dst`.

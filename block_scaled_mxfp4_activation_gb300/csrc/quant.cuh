@@ -1,7 +1,7 @@
 // MXFP4 block quantization arithmetic shared by the standalone quantize kernel
-// (four adjacent lanes own one 32-element block, 8 bf16 values each, and
-// combine their maxima with two butterfly shuffles) and the fused GEMM's
-// activation producer (two lanes per block, 16 values each, one shuffle).
+// and the fused GEMM's activation producer: in both, two adjacent lanes own
+// one 32-element block, 16 bf16 values each, and combine their maxima with
+// one shuffle.
 //
 // Rule (amd-mxfp4-mm submission 748756, `hw_pack_mxfp4`; submission 755056,
 // "Software MXFP4 quant"): amax = max |x| over the block; u = (bits(amax) +
@@ -16,17 +16,6 @@
 
 namespace mxfp4 {
 
-// Largest |x| of 8 bf16 values, as a bf16 bit pattern (sign cleared).  Works
-// on the integer patterns: for non-negative finite floats the integer order
-// is the numeric order, and nothing is flushed to zero.
-__device__ __forceinline__ uint32_t absmax8_bf16(uint4 v) {
-  const uint32_t m = 0x7FFF7FFFu;
-  uint32_t a = __vmaxu2(v.x & m, v.y & m);
-  uint32_t b = __vmaxu2(v.z & m, v.w & m);
-  a = __vmaxu2(a, b);
-  return max(a & 0xFFFFu, a >> 16);
-}
-
 // E8M0 byte of a block from its amax (bf16 bit pattern).
 __device__ __forceinline__ uint32_t scale_byte_from_amax(uint32_t amax_bf16) {
   const uint32_t u = ((amax_bf16 << 16) + 0x200000u) & 0xFF800000u;
@@ -35,7 +24,10 @@ __device__ __forceinline__ uint32_t scale_byte_from_amax(uint32_t amax_bf16) {
   return static_cast<uint32_t>(s + 127);
 }
 
-// Largest |x| of 16 bf16 values (two 16-byte words), as a bf16 bit pattern.
+// Largest |x| of 16 bf16 values (two 16-byte words), as a bf16 bit pattern
+// (sign cleared).  Works on the integer patterns: for non-negative finite
+// floats the integer order is the numeric order, and nothing is flushed to
+// zero.
 __device__ __forceinline__ uint32_t absmax16_bf16(uint4 v, uint4 w) {
   const uint32_t m = 0x7FFF7FFFu;
   uint32_t a = __vmaxu2(v.x & m, v.y & m);
@@ -84,18 +76,6 @@ __device__ __forceinline__ uint32_t e2m1_pack8(uint4 v, uint16_t scale_bf16) {
       : "=r"(out)
       : "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "h"(scale_bf16));
   return out;
-}
-
-// Quantizes the 8 values a lane owns as part of a 32-element block spread over
-// the 4 lanes lane^1, lane^2, lane^3 (all 32 lanes must call it together).
-// Returns the 4 code bytes; *byte_out receives the block's scale byte.
-__device__ __forceinline__ uint32_t quantize_quad(uint4 v, uint32_t* byte_out) {
-  uint32_t amax = absmax8_bf16(v);
-  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-  const uint32_t byte = scale_byte_from_amax(amax);
-  *byte_out = byte;
-  return e2m1_pack8(v, scale_bf16_from_byte(byte));
 }
 
 }  // namespace mxfp4

@@ -22,39 +22,49 @@ uint32_t* device_error_word() {
 }
 
 // ----------------------------------------------------------------------------- quantize
-// One thread per 8 consecutive elements of a row; 4 lanes per 32-element block;
-// a warp covers 256 consecutive elements (512 contiguous bytes of A).  Rows are
-// K/8 units long and K % 32 == 0, so a block never straddles two rows and the
-// lanes of a block are always all in or all out of range.
+// One thread per 16 consecutive elements of a row (two 16-byte loads in
+// flight); 2 lanes per 32-element block, combining their maxima with one
+// shuffle; a warp covers 512 consecutive elements (1 KB of A).  Rows are K/16
+// units long and K % 32 == 0, so a block never straddles two rows and both
+// lanes of a block are always in or out of range together.  (On GB300 this
+// beat 4 lanes of 8 elements by ~0.25 us per call at M = 64 and 256: half the
+// threads, the same load latency.)
 __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ A, int64_t M,
                                                        int64_t K, int64_t lda,
                                                        uint8_t* __restrict__ Aq,
                                                        uint8_t* __restrict__ As) {
-  const int64_t units_per_row = K / 8;
+  const int64_t units_per_row = K / 16;
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool valid = unit < M * units_per_row;
   const int64_t row = valid ? unit / units_per_row : 0;
   const int64_t j = valid ? unit - row * units_per_row : 0;
-  const uint16_t* src = A + row * lda + j * 8;
+  const uint16_t* src = A + row * lda + j * 16;
   // Under programmatic launch the next kernel may start its prologue now; this
   // one touches A and its outputs only once the previous grid has completed
   // (the outputs may still be read by it), after an L2 prefetch of its line.
   grid_launch_dependents();
-  if (valid && (j & 7) == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+  if (valid && (j & 3) == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
   grid_dependency_wait();
-  uint4 v = make_uint4(0, 0, 0, 0);
-  if (valid) v = __ldg(reinterpret_cast<const uint4*>(src));
-  uint32_t byte;
-  const uint32_t codes = quantize_quad(v, &byte);  // every lane takes part in the shuffles
+  uint4 v = make_uint4(0, 0, 0, 0), w = make_uint4(0, 0, 0, 0);
   if (valid) {
-    *reinterpret_cast<uint32_t*>(Aq + row * (K / 2) + j * 4) = codes;
-    if ((j & 3) == 0) As[row * (K / 32) + j / 4] = static_cast<uint8_t>(byte);
+    v = ld_after_wait_v4(src);  // A may be the previous grid's output
+    w = ld_after_wait_v4(src + 8);
+  }
+  // every lane takes part in the shuffle
+  uint32_t amax = absmax16_bf16(v, w);
+  amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+  const uint32_t byte = scale_byte_from_amax(amax);
+  const uint16_t sbf = scale_bf16_from_byte(byte);
+  const uint32_t c0 = e2m1_pack8(v, sbf), c1 = e2m1_pack8(w, sbf);
+  if (valid) {
+    *reinterpret_cast<uint2*>(Aq + row * (K / 2) + j * 8) = make_uint2(c0, c1);
+    if ((j & 1) == 0) As[row * (K / 32) + j / 2] = static_cast<uint8_t>(byte);
   }
 }
 
 cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
                             bool programmatic, cudaStream_t s) {
-  const int64_t units = M * (K / 8);
+  const int64_t units = M * (K / 16);
   const int threads = 256;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(static_cast<unsigned>(ceil_div(units, threads)), 1, 1);

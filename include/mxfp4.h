@@ -162,19 +162,22 @@ mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked,
 
 /* The fused entry for activations and results in host memory: uploads A
  * (host bf16 [M, lda_host]) into A_dev (device bf16 [M, lda_dev]), runs
- * mxfp4_quant_gemm on it (C_dev, ws as there) and downloads C_dev into C_host
- * (host bf16 [M, N]) -- three asynchronous operations on `stream`, issued by
- * one call.  The caller owns every buffer; host buffers should be pinned
- * (page-locked) for the copies to be asynchronous.  Pinned buffers that the
- * device can address (mapped host memory, with 16-byte aligned rows: lda_host
- * a multiple of 8, M*N a multiple of 8) are copied by the library's own copy
- * kernel, SM threads reading and writing host memory over the host link; any
- * other host buffer by cudaMemcpy*Async.  The upload reads A_host as soon as
- * its kernel starts (under programmatic launch possibly while the previous
- * kernel on the stream still runs), so A_host must hold the input when the
- * call is made -- the same rule as for any asynchronous copy from it.  C_host
- * is complete when the stream is.  All checks precede the upload: an error
- * launches nothing. */
+ * mxfp4_quant_gemm on it (C_dev, ws as there) and delivers the result to both
+ * C_dev and C_host (host bf16 [M, N]) -- asynchronous operations on `stream`,
+ * issued by one call.  The caller owns every buffer; host buffers should be
+ * pinned (page-locked) for the transfers to be asynchronous.
+ *   - A_host pinned and addressable by the device (mapped host memory) with
+ *     16-byte aligned rows (lda_host a multiple of 8): uploaded by the
+ *     library's copy kernel, SM threads reading host memory over the host
+ *     link; otherwise by cudaMemcpy2DAsync.
+ *   - C_host mapped and 16-byte aligned: written by the GEMM kernel itself,
+ *     beside C_dev (no download pass); otherwise C_dev is downloaded by
+ *     cudaMemcpyAsync after the GEMM.
+ * The upload reads A_host as soon as its kernel starts (under programmatic
+ * launch possibly while the previous kernel on the stream still runs), so
+ * A_host must hold the input when the call is made -- the same rule as for
+ * any asynchronous copy from it.  C_host is complete when the stream is.  All
+ * checks precede the upload: an error launches nothing. */
 mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void* A_dev, int64_t lda_dev,
                                      const void* Bpacked, void* C_dev, void* C_host, int64_t M, int64_t N,
                                      int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream);

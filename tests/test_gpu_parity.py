@@ -379,16 +379,26 @@ def test_gemm_full_size_sampled(oracle_mod, name):
 
 @pytest.mark.parametrize("pinned", [True, False])
 def test_quant_gemm_host_buffers(oracle_mod, pinned):
-    """Host activation in, host result out, one call: pinned buffers go through
-    the library's SM copy kernel, pageable ones through cudaMemcpy; row pitches
-    that break 16-byte alignment (lda 516) take the copy engines too.  Several
-    calls back to back with different inputs and no synchronisation between
-    them, every result checked (a copy reading too early or writing too late
-    shows as a stale or torn result)."""
-    for M, N, K, lda in ((32, 512, 512, 520), (64, 384, 1024, 1024), (5, 264, 512, 516), (3, 131, 256, 256)):
+    """Host activation in, host result out, one call.  Pinned buffers: the
+    activation goes up through the library's SM copy kernel and the GEMM kernel
+    writes the result into host memory itself, beside C_dev, on each of its
+    store paths (TMA-store tile, direct stores for N % 8 != 0, the split-K
+    reduction with 8-byte and with scalar stores, the two-pass route's GEMM);
+    pageable ones go through cudaMemcpy, and so do row pitches that break
+    16-byte alignment (lda 516).  Several calls back to back with different
+    inputs and no synchronisation between them, every result checked against
+    the device entry (a copy reading too early or writing too late shows as a
+    stale or torn result)."""
+    cases = ((32, 512, 512, 520, False), (64, 384, 1024, 1024, True), (5, 264, 512, 516, False),
+             (3, 131, 256, 256, False), (16, 264, 4096, 4096, False), (7, 131, 4096, 4096, False))
+    split_cases = 0
+    for M, N, K, lda, with_ws in cases:
         W = mx.quantize_weights(workloads.make_random(M, N, K, seed=M + K)[1].cuda())
         Ad = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
         Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+        ws = torch.empty(max(mx.workspace_bytes(M, N, K), 1), dtype=torch.uint8, device="cuda") if with_ws else None
+        plan = mx.gemm_plan(M, N, K, fused=True)
+        split_cases += plan["splits"] > 1
         calls = 4
         hosts_A, hosts_C, expect = [], [], []
         for c in range(calls):
@@ -400,14 +410,16 @@ def test_quant_gemm_host_buffers(oracle_mod, pinned):
                 Ah, Ch = Ah.pin_memory(), Ch.pin_memory()
             hosts_A.append(Ah[:, :K])
             hosts_C.append(Ch)
-            expect.append(mx.quant_gemm(A.cuda(), W).cpu())
+            expect.append(mx.quant_gemm(A.cuda(), W, workspace=ws).cpu())
         torch.cuda.synchronize()
         for c in range(calls):
-            mx.quant_gemm_host(hosts_A[c], W, Ad, Cd, hosts_C[c])
+            mx.quant_gemm_host(hosts_A[c], W, Ad, Cd, hosts_C[c], workspace=ws)
         torch.cuda.synchronize()
         assert torch.equal(Ad.cpu(), hosts_A[-1].contiguous())
+        assert torch.equal(Cd.cpu(), expect[-1])
         for c in range(calls):
             assert torch.equal(hosts_C[c], expect[c]), f"M={M} N={N} K={K} lda={lda} call {c}"
+    assert split_cases >= 2  # the split-K store path ran, with and without 8-byte stores
 
 
 # ----------------------------------------------------------------------------- bounded waits
