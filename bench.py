@@ -216,19 +216,32 @@ def time_graph_steps(prob: Problem, steps: int, warmup: int, stream: torch.cuda.
     return start.elapsed_time(end)
 
 
-def time_e2e(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream) -> float:
-    """Per step, one call of the public host-buffer entry (mxfp4_quant_gemm_host):
-    pinned host A -> device, the fused layer, device C -> pinned host.  Eager
-    launches, no graph.  Returns ms."""
+def time_e2e(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, via: str = "c_abi") -> float:
+    """Per step, one call of the host-buffer entry mxfp4_quant_gemm_host: pinned
+    host A -> device, the fused layer, C -> pinned host (and C_dev).  Eager
+    launches, no graph.  via="c_abi": the exported C function itself, called
+    through ctypes with the step's arguments prepared once (the call a C or C++
+    user makes); via="python": the package's Python wrapper, which checks and
+    marshals torch tensors on every call.  Returns ms."""
     w = prob.w
     hostA = prob.A[0].cpu().pin_memory()
     hostC = torch.empty((w.M, w.N), dtype=torch.bfloat16).pin_memory()
     devA = torch.empty_like(prob.A[0])
     devC = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=devA.device)
     mx = prob.mx
+    if via == "c_abi":
+        fn = mx.load_library().mxfp4_quant_gemm_host
+        args = [(hostA.data_ptr(), w.K, devA.data_ptr(), w.K, prob.W[j].data.data_ptr(), devC.data_ptr(),
+                 hostC.data_ptr(), w.M, w.N, w.K, prob.ws.data_ptr(), prob.ws.numel(), int(stream.cuda_stream))
+                for j in range(prob.copies)]
 
-    def step(i):
-        mx.quant_gemm_host(hostA, prob.W[i % prob.copies], devA, devC, hostC, workspace=prob.ws, stream=stream)
+        def step(i):
+            status = fn(*args[i % prob.copies])
+            if status:
+                raise mx.MXFP4Error(status, "mxfp4_quant_gemm_host")
+    else:
+        def step(i):
+            mx.quant_gemm_host(hostA, prob.W[i % prob.copies], devA, devC, hostC, workspace=prob.ws, stream=stream)
 
     for i in range(warmup):
         step(i)
@@ -357,8 +370,9 @@ def run_ours(args) -> dict:
     ms_warm = time_graph_steps(prob, min(args.steps, 2000), warmup, stream, rotate=False)
     us_warm = ms_warm * 1e3 / min(args.steps, 2000)
     e2e_steps = min(args.steps, 500)
-    ms_e2e = time_e2e(prob, e2e_steps, warmup, stream)
+    ms_e2e = time_e2e(prob, e2e_steps, warmup, stream, via="c_abi")
     us_e2e = ms_e2e * 1e3 / e2e_steps
+    us_e2e_py = time_e2e(prob, e2e_steps, warmup, stream, via="python") * 1e3 / e2e_steps
     err = mx.device_error(reset=True)
     if err:
         raise RuntimeError(f"device error word {err:#x} after timing")
@@ -386,7 +400,11 @@ def run_ours(args) -> dict:
         "warm_l2_us_per_call": round(us_warm, 4),
         "e2e": {"value": round(us_e2e, 3), "unit": UNIT, "h2d_bytes_per_step": 2 * w.M * w.K,
                 "d2h_bytes_per_step": 2 * w.M * w.N,
-                "how": "mxfp4_quant_gemm_host per step: pinned A -> device, fused layer, C -> pinned host; eager"},
+                "how": "the C-ABI call mxfp4_quant_gemm_host per step (through ctypes, arguments prepared once): "
+                       "pinned host A -> device, fused layer, C -> pinned host; eager launches",
+                "python_api_value": round(us_e2e_py, 3),
+                "python_api_how": "the same step through the Python wrapper quant_gemm_host (tensor checks and "
+                                  "marshalling on every call)"},
         "gpu_launches": args.steps,
         "clocks": clocks,
     }

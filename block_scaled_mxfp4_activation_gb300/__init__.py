@@ -109,14 +109,13 @@ def status_string(status: int) -> str:
 _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 
 
-def _stream(stream=None, device: torch.device | None = None) -> int:
+def _stream(stream=None, t: torch.Tensor | None = None) -> int:
     """The CUDA stream handle to launch on: `stream`, else torch's current
-    stream of `device` (or of the current device)."""
+    stream of the device of CUDA tensor `t` (or of the current device)."""
     if stream is not None:
         return int(stream.cuda_stream)
     if _raw_stream is not None:  # the handle without building a Stream object
-        idx = device.index if device is not None and device.index is not None else torch.cuda.current_device()
-        return int(_raw_stream(idx))
+        return int(_raw_stream(t.get_device() if t is not None else torch.cuda.current_device()))
     return int(torch.cuda.current_stream().cuda_stream)
 
 
@@ -127,7 +126,7 @@ def _ptr(t: torch.Tensor | None):
 def _call(name: str, *args):
     lib = _lib if _lib is not None else load_library()
     status = getattr(lib, name)(*args)
-    if status != MXFP4_OK:
+    if status:
         detail = lib.mxfp4_last_error_string().decode() if status == 5 else ""
         raise MXFP4Error(status, name, detail)
 
@@ -148,7 +147,7 @@ def quantize(A: torch.Tensor, out: tuple[torch.Tensor, torch.Tensor] | None = No
         out = (torch.empty((M, K // 2), dtype=torch.uint8, device=A.device),
                torch.empty((M, K // 32), dtype=torch.uint8, device=A.device))
     Aq, As = out
-    _call("mxfp4_quantize", _ptr(A), M, K, A.stride(0), _ptr(Aq), _ptr(As), _stream(stream, A.device))
+    _call("mxfp4_quantize", _ptr(A), M, K, A.stride(0), _ptr(Aq), _ptr(As), _stream(stream, A))
     return Aq, As
 
 
@@ -242,7 +241,7 @@ def gemm(Aq: torch.Tensor, As: torch.Tensor, W: PackedWeight, out: torch.Tensor 
         raise ValueError("Aq/As shapes do not match the weight's K")
     if out is None:
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=Aq.device)
-    _call("mxfp4_gemm", _ptr(Aq), _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K, None, 0, _stream(stream, Aq.device))
+    _call("mxfp4_gemm", _ptr(Aq), _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K, None, 0, _stream(stream, Aq))
     return out
 
 
@@ -255,18 +254,19 @@ def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
     allocator (none for small M).  Pass an explicit one to reuse it."""
     W = _weight(W)
     _need(A, torch.bfloat16, "A")
-    if A.dim() != 2 or A.shape[1] != W.K or A.stride(1) != 1:
+    shape, st = A.shape, A.stride()
+    if len(shape) != 2 or shape[1] != W.K or st[1] != 1:
         raise ValueError("A must be [M, K] with unit column stride")
-    M = A.shape[0]
+    M = shape[0]
     if out is None:
         out = torch.empty((M, W.N), dtype=torch.bfloat16, device=A.device)
     if workspace is None:
         nbytes = workspace_bytes(M, W.N, W.K)
         if nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=A.device)
-    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel()) if workspace is not None else (None, 0)
-    _call("mxfp4_quant_gemm", _ptr(A), A.stride(0), _ptr(W.data), _ptr(out), M, W.N, W.K, ws_ptr, ws_bytes,
-          _stream(stream, A.device))
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    _call("mxfp4_quant_gemm", A.data_ptr(), st[0], W.data.data_ptr(), out.data_ptr(), M, W.N, W.K, ws_ptr, ws_bytes,
+          _stream(stream, A))
     return out
 
 
@@ -276,14 +276,17 @@ def quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, 
     quantize + GEMM -> C_dev and C_host (pinned CPU bf16 [M, N], written by the GEMM kernel
     itself when the device can address it); asynchronous on the stream."""
     W = _weight(W)
+    strides = []
     for t, dev, what in ((A_host, False, "A_host"), (C_host, False, "C_host"), (A_dev, True, "A_dev"),
                          (C_dev, True, "C_dev")):
-        if not isinstance(t, torch.Tensor) or t.dtype != torch.bfloat16 or t.is_cuda != dev or t.stride(-1) != 1:
+        st = t.stride() if isinstance(t, torch.Tensor) else None
+        if st is None or t.dtype is not torch.bfloat16 or t.is_cuda is not dev or st[-1] != 1:
             raise TypeError(f"{what} must be a {'CUDA' if dev else 'CPU'} bf16 tensor with unit column stride")
+        strides.append(st[0])
     M = A_host.shape[0]
-    ws_ptr, ws_bytes = (_ptr(workspace), workspace.numel()) if workspace is not None else (None, 0)
-    _call("mxfp4_quant_gemm_host", _ptr(A_host), A_host.stride(0), _ptr(A_dev), A_dev.stride(0), _ptr(W.data),
-          _ptr(C_dev), _ptr(C_host), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream, A_dev.device))
+    ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
+    _call("mxfp4_quant_gemm_host", A_host.data_ptr(), strides[0], A_dev.data_ptr(), strides[2], W.data.data_ptr(),
+          C_dev.data_ptr(), C_host.data_ptr(), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream, A_dev))
     return C_host
 
 
