@@ -15,6 +15,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import math
 import os
@@ -62,11 +63,15 @@ def measured_peaks() -> dict:
 
 
 def source_hash() -> str:
+    """Hash of the CUDA sources' code: comments and whitespace are left out, so
+    a comment edit does not void counters taken on the same code."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_scaled_mxfp4_activation_gb300", "csrc")
     for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(f.encode() + fh.read())
+        with open(os.path.join(csrc, f), encoding="utf-8") as fh:
+            code = re.sub(r"/\*.*?\*/", " ", fh.read(), flags=re.S)
+        code = re.sub(r"//[^\n]*", " ", code)
+        h.update(f.encode() + " ".join(code.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -1,9 +1,10 @@
 // Row copies between any two buffers the GPU can address, done by SM threads:
-// the host-buffer entry (mxfp4_quant_gemm_host) moves its activation in and its
-// result out through these when the host buffers are pinned and mapped.  On a
-// GB300 node the GPU reaches host memory over the coherent NVLink-C2C link, and
-// a small copy done by SM loads and stores finishes well before a DMA copy of
-// the same size (which pays a fixed start-up latency of a few microseconds).
+// the host-buffer entry (mxfp4_quant_gemm_host) moves a pinned, mapped host
+// activation in through this (its result goes out from the GEMM kernel itself).
+// On a GB300 node the GPU reaches host memory over the coherent NVLink-C2C
+// link, and a small copy done by SM loads and stores finishes well before a DMA
+// copy of the same size (which pays a fixed start-up latency of a few
+// microseconds).
 #include "internal.h"
 #include "ptx.cuh"
 
