@@ -199,8 +199,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     const uint64_t policy_b = policy_evict_first();  // weights: read once per call
     const uint64_t policy_a = policy_evict_last();   // activations: shared by every N tile
     const int pre = min(stages, kt_count);
-    auto issue_w = [&](int i) {
-      const int s = i % stages, kt = kt_begin + i;
+    // K tile i of this split into stage s
+    auto issue_w = [&](int i, int s) {
+      const int kt = kt_begin + i;
       const uint32_t bar = full_w(s), dst_b = sbase + s * C::kBTileBytes, dst_sf = sbase + args.sfw_off + s * kSfTileBytes;
       const uint8_t* src_sf = args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes;
       if (leader) {
@@ -209,8 +210,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         bulk_load(dst_sf, src_sf, kSfTileBytes, bar, policy_b);
       }
     };
-    auto issue_a = [&](int i) {
-      const int s = i % stages, kt = kt_begin + i;
+    auto issue_a = [&](int i, int s) {
+      const int kt = kt_begin + i;
       const uint32_t bar = full_in(s);
       if constexpr (kFused) {
         const uint32_t dst = sbase + args.abf_off + s * args.abf_stage_bytes;
@@ -227,7 +228,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       }
     };
     if (args.weights_early) {
-      for (int i = 0; i < pre; ++i) issue_w(i);
+      for (int i = 0; i < pre; ++i) issue_w(i, i);
     } else {
       for (int i = 0; i < kt_count; ++i) {
         const int kt = kt_begin + i;
@@ -244,19 +245,19 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     }
     grid_dependency_wait();
     if (!args.weights_early)
-      for (int i = 0; i < pre; ++i) issue_w(i);
-    for (int i = 0; i < pre; ++i) issue_a(i);
+      for (int i = 0; i < pre; ++i) issue_w(i, i);
+    for (int i = 0; i < pre; ++i) issue_a(i, i);
     if (args.trigger_late) grid_launch_dependents();
     int issued = pre;
-    for (int i = pre; i < kt_count; ++i) {
-      const int s = i % stages, round = i / stages;
+    // (pre == stages whenever this loop runs: it starts at stage 0 of round 1)
+    for (int i = pre, s = 0, round = 1; i < kt_count; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty(s), (round - 1) & 1, timeout))) {
         if (leader) report_error(args.err, kErrWaitEmpty);
         *abort_flag = 1u;
       }
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
-      issue_w(i);
-      issue_a(i);
+      issue_w(i, s);
+      issue_a(i, s);
       issued = i + 1;
     }
     // Before the CTA can exit, every copy it issued must have landed.
@@ -297,8 +298,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     const int pre = min(stages, kt_count);
     bool alive = true;
     for (int i = 0; i < pre && alive; ++i) alive = weight_scales(i, 0);
-    for (int i = 0; i < kt_count && alive; ++i) {
-      const int s = i % stages, round = i / stages;
+    for (int i = 0, s = 0, round = 0; i < kt_count && alive; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
       const uint32_t sfw_t = tmem_sf + s * C::kSfCols;
       const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
       const uint32_t sfa_s = sbase + args.sfa_off + s * C::kSfaStageBytes;
@@ -341,8 +341,12 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   } else {
     // ------------------------------------------------------------------ activation producer
     const int tid = threadIdx.x - 64;
-    grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
+    // the kernel arguments the loop reads, fetched before the wait (a first
+    // read of a parameter can miss the constant cache)
+    const uint32_t a_off = args.a_off, sfa_off = args.sfa_off, abf_off = args.abf_off;
+    const uint32_t abf_stage_bytes = args.abf_stage_bytes;
     bool triggered = !args.trigger_late;
+    grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
     const int64_t nblk = args.K / 32;
     // unfused: the 8 scale bytes of row `tid` for K tile i (one row per thread;
     // block_m <= 256 = the producer thread count): one 8-byte load when rows
@@ -373,8 +377,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
           if (i < kt_count) load_scales(i, sc_pre[i][0], sc_pre[i][1]);
       }
     }
-    for (int i = 0; i < kt_count; ++i) {
-      const int s = i % stages, round = i / stages;
+    for (int i = 0, s = 0, round = 0; i < kt_count; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
       if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
         report_error(args.err, kErrWaitEmpty);
         *abort_flag = 1u;
@@ -388,10 +391,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         triggered = true;
       }
       if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;  // warp-uniform: the shuffles below need every lane
-      uint8_t* a_tile = smem + args.a_off + s * C::kATileBytes;
-      uint8_t* sfa = smem + args.sfa_off + s * C::kSfaStageBytes;
+      uint8_t* a_tile = smem + a_off + s * C::kATileBytes;
+      uint8_t* sfa = smem + sfa_off + s * C::kSfaStageBytes;
       if constexpr (kFused) {
-        const uint8_t* abf = smem + args.abf_off + s * args.abf_stage_bytes;
+        const uint8_t* abf = smem + abf_off + s * abf_stage_bytes;
         if (m_valid >= BM)
           quantize_tile<BM, C::kAThreads, C::kRowChunks, false>(abf, a_tile, sfa, tid, m_valid);
         else
