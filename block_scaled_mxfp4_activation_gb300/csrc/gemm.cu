@@ -435,6 +435,26 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     const int qr = warp & 3;           // TMEM lanes this warp may read
     const int h = (warp - 2) >> 2;     // which half of the column chunks
     const int chunks = (m_valid + 15) >> 4;
+    if (splits == 1 && args.c_tma && chunks == 1 && nacc == 1) {
+      // one 16-row chunk (block_m 16, or M <= 16): both warp halves load it,
+      // each converts and stages 8 of its rows, so all eight epilogue warps work
+      uint32_t r[16];
+      if (have) {
+        tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(qr * 32) << 16), r);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int e = 0; e < 16; ++e) r[e] = 0u;
+      }
+      __nv_bfloat16* cs = reinterpret_cast<__nv_bfloat16*>(smem) + (h * 8) * kTileN + qr * 32 + lane;
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const uint32_t lo = h ? r[8 + e] : r[e], hi = h ? r[9 + e] : r[e + 1];
+        const __nv_bfloat162 pr = __floats2bfloat162_rn(__uint_as_float(lo), __uint_as_float(hi));
+        cs[e * kTileN] = pr.x;
+        cs[(e + 1) * kTileN] = pr.y;
+      }
+    } else
 #pragma unroll 1
     for (int c = h; c < chunks; c += 2) {
       uint32_t r[16];
