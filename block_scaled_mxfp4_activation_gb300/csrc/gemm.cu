@@ -249,7 +249,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     for (int i = 0; i < pre; ++i) issue_a(i, i);
     if (args.trigger_late) grid_launch_dependents();
     int issued = pre;
-    // (pre == stages whenever this loop runs: it starts at stage 0 of round 1)
+    // (pre == stages whenever this loop runs: it starts over at stage 0, on the
+    // stages' second fill)
     for (int i = pre, s = 0, round = 1; i < kt_count; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
       if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty(s), (round - 1) & 1, timeout))) {
         if (leader) report_error(args.err, kErrWaitEmpty);
