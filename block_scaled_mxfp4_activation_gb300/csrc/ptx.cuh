@@ -332,13 +332,4 @@ __device__ __forceinline__ float4 ld_shared_f4(uint32_t saddr) {
   return v;
 }
 
-__device__ __forceinline__ float4 ld_cluster_f4(uint32_t caddr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(caddr)
-               : "memory");
-  return v;
-}
-
 }  // namespace mxfp4
