@@ -84,6 +84,11 @@ def test_argument_checks_launch_nothing(lib):
     assert lib.mxfp4_quant_gemm(fake, 68, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED  # lda % 8
     assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 4, 0, 64, None, 0, None) == INVALID
     assert lib.mxfp4_quant_gemm(fake, 1 << 40, fake, fake, 1 << 31, 128, 1 << 31, None, 0, None) == UNSUPPORTED
+    # sizes past the library's limits (32-bit in-kernel indices), on every compute entry
+    assert lib.mxfp4_quantize(fake, 1 << 40, 64, 64, fake, fake, None) == UNSUPPORTED
+    assert lib.mxfp4_gemm(fake, fake, fake, fake, 4, 1 << 40, 64, None, 0, None) == UNSUPPORTED
+    assert lib.mxfp4_gemm(fake, fake, fake, fake, 1 << 20, 1 << 20, 64, None, 0, None) == UNSUPPORTED  # M*N > 2^31
+    assert lib.mxfp4_quant_gemm_host(fake, 64, fake, 64, fake, fake, fake, 4, 1 << 40, 64, None, 0, None) == UNSUPPORTED
     assert lib.mxfp4_quant_gemm_host(None, 64, fake, 64, fake, fake, fake, 4, 128, 64, None, 0, None) == INVALID
     assert lib.mxfp4_quant_gemm_host(fake, 64, fake, 68, fake, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED
     assert lib.mxfp4_quant_gemm_host(fake, 64, odd, 64, fake, fake, fake, 4, 128, 64, None, 0, None) == MISALIGNED
