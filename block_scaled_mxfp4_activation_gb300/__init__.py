@@ -25,6 +25,7 @@ __all__ = [
     "pack_weights", "pack_weights_shuffled", "unpack_weights", "quantize_weights", "gemm", "quant_gemm", "gemm_plan",
     "gemm_with_plan", "workspace_bytes", "device_error", "set_wait_timeout_ns", "diag_wait_timeout",
     "status_string", "Plan", "set_programmatic_launch", "custom_kernel", "quant_gemm_host",
+    "PreparedCall", "prepare_quant_gemm", "prepare_quant_gemm_host",
 ]
 
 MXFP4_OK = 0
@@ -245,13 +246,9 @@ def gemm(Aq: torch.Tensor, As: torch.Tensor, W: PackedWeight, out: torch.Tensor 
     return out
 
 
-def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
-               stream=None) -> torch.Tensor:
-    """The fused layer: bf16 A [M, K] -> quantized -> x packed W -> bf16 C [M, N].
-
-    `workspace` (uint8 CUDA tensor) lets large-M calls take the two-pass route;
-    when None, one of workspace_bytes(M, N, K) bytes is taken from torch's
-    allocator (none for small M).  Pass an explicit one to reuse it."""
+def _quant_gemm_args(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None, workspace: torch.Tensor | None,
+                     stream) -> tuple:
+    """Checks and marshals mxfp4_quant_gemm's arguments; returns (C args, out, workspace)."""
     W = _weight(W)
     _need(A, torch.bfloat16, "A")
     shape, st = A.shape, A.stride()
@@ -265,16 +262,25 @@ def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None
         if nbytes:
             workspace = torch.empty(nbytes, dtype=torch.uint8, device=A.device)
     ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
-    _call("mxfp4_quant_gemm", A.data_ptr(), st[0], W.data.data_ptr(), out.data_ptr(), M, W.N, W.K, ws_ptr, ws_bytes,
-          _stream(stream, A))
+    args = (A.data_ptr(), st[0], W.data.data_ptr(), out.data_ptr(), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream, A))
+    return args, out, workspace
+
+
+def quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None, workspace: torch.Tensor | None = None,
+               stream=None) -> torch.Tensor:
+    """The fused layer: bf16 A [M, K] -> quantized -> x packed W -> bf16 C [M, N].
+
+    `workspace` (uint8 CUDA tensor) lets large-M calls take the two-pass route;
+    when None, one of workspace_bytes(M, N, K) bytes is taken from torch's
+    allocator (none for small M).  Pass an explicit one to reuse it."""
+    args, out, _ = _quant_gemm_args(A, W, out, workspace, stream)
+    _call("mxfp4_quant_gemm", *args)
     return out
 
 
-def quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, C_dev: torch.Tensor,
-                    C_host: torch.Tensor, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """The fused layer on host data in one call: A_host (pinned CPU bf16 [M, K]) -> A_dev ->
-    quantize + GEMM -> C_dev and C_host (pinned CPU bf16 [M, N], written by the GEMM kernel
-    itself when the device can address it); asynchronous on the stream."""
+def _quant_gemm_host_args(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, C_dev: torch.Tensor,
+                          C_host: torch.Tensor, workspace: torch.Tensor | None, stream) -> tuple:
+    """Checks and marshals mxfp4_quant_gemm_host's arguments."""
     W = _weight(W)
     strides = []
     for t, dev, what in ((A_host, False, "A_host"), (C_host, False, "C_host"), (A_dev, True, "A_dev"),
@@ -285,9 +291,59 @@ def quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, 
         strides.append(st[0])
     M = A_host.shape[0]
     ws_ptr, ws_bytes = (workspace.data_ptr(), workspace.numel()) if workspace is not None else (None, 0)
-    _call("mxfp4_quant_gemm_host", A_host.data_ptr(), strides[0], A_dev.data_ptr(), strides[2], W.data.data_ptr(),
-          C_dev.data_ptr(), C_host.data_ptr(), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream, A_dev))
+    return (A_host.data_ptr(), strides[0], A_dev.data_ptr(), strides[2], W.data.data_ptr(), C_dev.data_ptr(),
+            C_host.data_ptr(), M, W.N, W.K, ws_ptr, ws_bytes, _stream(stream, A_dev))
+
+
+def quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, C_dev: torch.Tensor,
+                    C_host: torch.Tensor, workspace: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """The fused layer on host data in one call: A_host (pinned CPU bf16 [M, K]) -> A_dev ->
+    quantize + GEMM -> C_dev and C_host (pinned CPU bf16 [M, N], written by the GEMM kernel
+    itself when the device can address it); asynchronous on the stream."""
+    _call("mxfp4_quant_gemm_host", *_quant_gemm_host_args(A_host, W, A_dev, C_dev, C_host, workspace, stream))
     return C_host
+
+
+class PreparedCall:
+    """One library call with its arguments checked and marshalled once.
+
+    Calling it launches the same operation again on the same buffers and stream,
+    with no per-call tensor checks: for loops that run one layer many times on
+    fixed buffers (the same contract as replaying a captured CUDA graph).  It
+    holds references to its tensors; the caller must not resize or reallocate
+    them while the call is in use (new data in the same buffers is fine)."""
+
+    def __init__(self, name: str, args: tuple, keep: tuple, result=None):
+        self._fn = getattr(load_library(), name)
+        self._name = name
+        self._args = args
+        self._keep = keep
+        self.result = result
+
+    def __call__(self):
+        status = self._fn(*self._args)
+        if status:
+            lib = load_library()
+            detail = lib.mxfp4_last_error_string().decode() if status == 5 else ""
+            raise MXFP4Error(status, self._name, detail)
+        return self.result
+
+
+def prepare_quant_gemm(A: torch.Tensor, W: PackedWeight, out: torch.Tensor | None = None,
+                       workspace: torch.Tensor | None = None, stream=None) -> PreparedCall:
+    """quant_gemm bound to these buffers: `call()` runs the fused layer on whatever A
+    holds and returns `out` (allocated here when None, as is the workspace)."""
+    args, out, workspace = _quant_gemm_args(A, W, out, workspace, stream)
+    return PreparedCall("mxfp4_quant_gemm", args, (A, W, out, workspace), out)
+
+
+def prepare_quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.Tensor, C_dev: torch.Tensor,
+                            C_host: torch.Tensor, workspace: torch.Tensor | None = None,
+                            stream=None) -> PreparedCall:
+    """quant_gemm_host bound to these buffers: `call()` moves A_host in, runs the layer and
+    delivers C to C_dev and C_host, returning C_host."""
+    args = _quant_gemm_host_args(A_host, W, A_dev, C_dev, C_host, workspace, stream)
+    return PreparedCall("mxfp4_quant_gemm_host", args, (A_host, W, A_dev, C_dev, C_host, workspace), C_host)
 
 
 def gemm_plan(M: int, N: int, K: int, fused: bool = True) -> dict:

@@ -106,3 +106,15 @@ def test_python_binding_refuses_cpu_tensors():
         mx.quantize(torch.zeros(4, 64, dtype=torch.bfloat16))
     with pytest.raises(TypeError):
         mx.quant_gemm(torch.zeros(4, 64, dtype=torch.bfloat16), mx.PackedWeight(torch.zeros(8, dtype=torch.uint8), 128, 64))
+
+
+def test_prepared_calls_check_their_arguments_once():
+    import torch
+
+    W = mx.PackedWeight(torch.zeros(8, dtype=torch.uint8), 128, 64)
+    cpu = torch.zeros(4, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        mx.prepare_quant_gemm(cpu, W)
+    with pytest.raises(TypeError):  # A_dev on the host
+        mx.prepare_quant_gemm_host(cpu, W, cpu, cpu, torch.zeros(4, 128, dtype=torch.bfloat16))
+

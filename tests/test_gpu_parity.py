@@ -422,6 +422,33 @@ def test_quant_gemm_host_buffers(oracle_mod, pinned):
     assert split_cases >= 2  # the split-K store path ran, with and without 8-byte stores
 
 
+def test_prepared_calls_match_the_per_call_entries(oracle_mod):
+    """A prepared call re-runs its layer on whatever its buffers hold: new inputs
+    written into the same buffers between calls give the per-call entries'
+    results (device entry, and host entry with pinned buffers)."""
+    M, N, K = 32, 512, 1024
+    W = mx.quantize_weights(workloads.make_random(M, N, K, seed=5)[1].cuda())
+    A = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    C = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Ah = torch.empty((M, K), dtype=torch.bfloat16).pin_memory()
+    Ad = torch.empty((M, K), dtype=torch.bfloat16, device="cuda")
+    Cd = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    Ch = torch.empty((M, N), dtype=torch.bfloat16).pin_memory()
+    dev_call = mx.prepare_quant_gemm(A, W, out=C)
+    host_call = mx.prepare_quant_gemm_host(Ah, W, Ad, Cd, Ch)
+    for c in range(3):
+        x = workloads.make_random(M, N, K, seed=50 + c)[0]
+        A.copy_(x)
+        Ah.copy_(x)
+        torch.cuda.synchronize()
+        assert dev_call() is C
+        assert host_call() is Ch
+        torch.cuda.synchronize()
+        ref = mx.quant_gemm(x.cuda(), W)
+        assert torch.equal(C, ref), f"device entry, call {c}"
+        assert torch.equal(Ch, ref.cpu()) and torch.equal(Cd, ref), f"host entry, call {c}"
+
+
 # ----------------------------------------------------------------------------- bounded waits
 def test_bounded_wait_reports_instead_of_hanging():
     assert mx.device_error(reset=True) == 0
