@@ -7,7 +7,11 @@ batch: A bf16 [M, K] quantized in-kernel, times a pre-packed MXFP4 weight
 Timing: a CUDA graph of R calls, call i on copy i % R of both A and the packed
 weight, with R chosen so that the copies exceed twice the L2 cache (every call
 streams its operands from HBM); the graph is replayed until exactly K steps
-ran, bracketed by CUDA events on the replay stream.  Prints one JSON line.
+ran, bracketed by CUDA events on the replay stream, with an L2-sized write
+enqueued just before the start event.  Per shape, beside this pipelined
+figure: the same calls without overlap between consecutive calls (a lone
+call's latency) and the per-layer time of a dependent chain of layers.
+Prints one JSON line.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 """
@@ -143,6 +147,19 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------- our arm
+ALL_WORKLOADS = {**workloads.WORKLOADS, **workloads.EXTRA_WORKLOADS}
+
+L2_METHOD = ("each timed pass streams rotating copies of A and the packed weight totalling more than 2x L2, and an "
+             "L2-sized write precedes the timed region")
+
+
+def bench_config(w: workloads.Workload) -> dict:
+    """The `config` of both arms' JSON lines for one workload (one dict, so the
+    two arms' lines compare equal)."""
+    return {"workload": f"{w.name}: fused bf16->MXFP4 quantize + block-scaled MXFP4 GEMM, bf16 out, {w.label}",
+            "M": w.M, "N": w.N, "K": w.K, "seed": w.seed, "l2": L2_METHOD}
+
+
 class Problem:
     """R rotating copies of A and of the packed weight for one workload."""
 
@@ -164,17 +181,59 @@ class Problem:
         self.ws = torch.empty(max(mx.workspace_bytes(w.M, w.N, w.K), 1), dtype=torch.uint8, device=device)
         self.rotating_bytes = per_copy * self.copies
         self.l2 = l2
+        self.launches_per_call = 2 if mx.gemm_plan(w.M, w.N, w.K, fused=True)["two_pass"] else 1
+        self.flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
 
     def call(self, i: int):
         j = i % self.copies
         self.mx.quant_gemm(self.A[j], self.W[j], out=self.C[j], workspace=self.ws)
 
-    def graph(self, n: int, stream: torch.cuda.Stream, rotate: bool = True) -> torch.cuda.CUDAGraph:
+    def graph(self, n: int, stream: torch.cuda.Stream, first: int = 0, rotate: bool = True) -> torch.cuda.CUDAGraph:
+        """n calls on copies first, first + 1, ... (or all on copy 0)."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.stream(stream):
             with torch.cuda.graph(g, stream=stream):
                 for i in range(n):
-                    self.call(i if rotate else 0)
+                    self.call(first + i if rotate else 0)
+        return g
+
+
+class Chain:
+    """A dependent chain of layers at one workload's shape: layer 2i maps
+    [M, K] -> [M, N] with a weight [N, K], layer 2i+1 maps [M, N] -> [M, K]
+    with a weight [K, N] (an up- and a down-projection), each layer's output
+    the next layer's activation.  Every layer has its own weight copy, enough
+    that the weights of one pass exceed 2x L2; weights ~ N(0, 1/fan_in) keep
+    the activations' magnitude steady along the chain."""
+
+    def __init__(self, w: workloads.Workload, device: torch.device):
+        import block_scaled_mxfp4_activation_gb300 as mx
+
+        self.mx, self.w = mx, w
+        g = torch.Generator().manual_seed(w.seed + 77)
+        up = (torch.randn((w.N, w.K), generator=g) / math.sqrt(w.K)).to(torch.bfloat16).to(device)
+        down = (torch.randn((w.K, w.N), generator=g) / math.sqrt(w.N)).to(torch.bfloat16).to(device)
+        Wu, Wd = mx.quantize_weights(up), mx.quantize_weights(down)
+        l2 = int(getattr(torch.cuda.get_device_properties(device), "L2_cache_size", 128 << 20))
+        pairs = max(2, math.ceil(2 * l2 / (Wu.data.numel() + Wd.data.numel())))
+        self.layers = []
+        for _ in range(pairs):
+            self.layers.append(mx.PackedWeight(Wu.data.clone(), w.N, w.K))
+            self.layers.append(mx.PackedWeight(Wd.data.clone(), w.K, w.N))
+        A = workloads.make_inputs(w)[0].to(device)
+        self.x = A.clone()
+        self.y = torch.empty((w.M, w.N), dtype=torch.bfloat16, device=device)
+        nbytes = max(mx.workspace_bytes(w.M, w.N, w.K), mx.workspace_bytes(w.M, w.K, w.N), 1)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.flush = torch.empty(2 * l2, dtype=torch.uint8, device=device)
+
+    def graph(self, stream: torch.cuda.Stream) -> torch.cuda.CUDAGraph:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                for i, W in enumerate(self.layers):
+                    src, dst = (self.x, self.y) if i % 2 == 0 else (self.y, self.x)
+                    self.mx.quant_gemm(src, W, out=dst, workspace=self.ws)
         return g
 
 
@@ -192,33 +251,59 @@ def aggregate_over_ranks(ms_local: float, steps: int, world: int) -> tuple[float
     return ms_max, ms_max * 1e3 / (steps * world)
 
 
-def time_graph_steps(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, rotate: bool = True,
-                     barrier=None):
-    """Exactly `steps` calls (graph replays), after `warmup` calls; returns ms."""
-    R = prob.copies if rotate else 1
-    chunk = min(steps, max(R, 256))
-    full, rest = divmod(steps, chunk)
-    g_full = prob.graph(chunk, stream, rotate)
-    g_rest = prob.graph(rest, stream, rotate) if rest else None
-    g_warm = prob.graph(max(warmup, 1), stream, rotate)
-    with torch.cuda.stream(stream):
-        g_warm.replay()
+def _timed(replays, flush: torch.Tensor, stream: torch.cuda.Stream, barrier=None) -> float:
+    """ms of `replays()` (graph replays enqueued on `stream`) between CUDA events
+    on that stream.  An L2-sized write goes first: it leaves L2 holding none of
+    the operands, and it keeps the GPU busy while the host enqueues the events
+    and replays, so the timed region starts on the device with work queued."""
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     if barrier:
         barrier()
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    torch.cuda.synchronize()
     with torch.cuda.stream(stream):
+        flush.fill_(1)
         start.record(stream)
-        for _ in range(full):
-            g_full.replay()
-        if g_rest is not None:
-            g_rest.replay()
+        replays()
         end.record(stream)
     torch.cuda.synchronize()
     if barrier:
         barrier()
     return start.elapsed_time(end)
+
+
+def time_graph_steps(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, rotate: bool = True,
+                     barrier=None) -> float:
+    """Exactly `steps` calls (graph replays), after `warmup` untimed calls on
+    copies the timed calls do not start with (the last ones); returns ms."""
+    R = prob.copies if rotate else 1
+    chunk = min(steps, max(R, 256))
+    full, rest = divmod(steps, chunk)
+    g_full = prob.graph(chunk, stream, rotate=rotate)
+    g_rest = prob.graph(rest, stream, first=chunk, rotate=rotate) if rest else None
+    w = max(warmup, 1)
+    g_warm = prob.graph(w, stream, first=R - (w % R) if rotate else 0, rotate=rotate)
+    with torch.cuda.stream(stream):
+        g_warm.replay()
+    torch.cuda.synchronize()
+
+    def replays():
+        for _ in range(full):
+            g_full.replay()
+        if g_rest is not None:
+            g_rest.replay()
+
+    return _timed(replays, prob.flush, stream, barrier)
+
+
+def time_chain(chain: Chain, stream: torch.cuda.Stream, reps: int = 3) -> float:
+    """µs per layer of the dependent chain (median of `reps` timed passes after
+    one untimed pass)."""
+    g = chain.graph(stream)
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    times = [_timed(g.replay, chain.flush, stream) for _ in range(reps)]
+    return float(np.median(times)) * 1e3 / len(chain.layers)
 
 
 def time_e2e(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, via: str = "c_abi") -> float:
@@ -256,7 +341,7 @@ def time_e2e(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, 
             mx.quant_gemm_host(hostA, prob.W[i % prob.copies], devA, devC, hostC, workspace=prob.ws, stream=stream)
 
     for i in range(warmup):
-        step(i)
+        step(prob.copies - 1 - (i % prob.copies))
     torch.cuda.synchronize()
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     start.record(stream)
@@ -268,7 +353,7 @@ def time_e2e(prob: Problem, steps: int, warmup: int, stream: torch.cuda.Stream, 
 
 
 def shape_report(name: str, us: float, peaks: dict, fused: bool = True) -> dict:
-    w = workloads.WORKLOADS[name]
+    w = ALL_WORKLOADS[name]
     b = algorithmic_bytes(w.M, w.N, w.K, fused)
     gbs = b / (us * 1e-6) / 1e9
     tflops = flops(w.M, w.N, w.K) / (us * 1e-6) / 1e12
@@ -348,6 +433,30 @@ def cpu_baseline_all_cores(name: str, per_core_elems: int, cores: int | None = N
                       f"processes ({wall:.1f} s wall), scaled to M*N"}
 
 
+def latency_report(w: workloads.Workload, prob: Problem, stream: torch.cuda.Stream, warmup: int, n: int) -> dict:
+    """Beside the pipelined figure (independent calls, each overlapping the one
+    before it): the same calls with no overlap (programmatic launch off: every
+    call starts once the previous one has finished, the latency of a lone
+    call), and the per-layer time of a dependent chain (each layer's output is
+    the next layer's input), with overlap on and off."""
+    mx = prob.mx
+    out = {}
+    try:
+        mx.set_programmatic_launch(0)
+        out["us_per_call_no_overlap"] = round(time_graph_steps(prob, n, warmup, stream) * 1e3 / n, 4)
+        chain = Chain(w, prob.A[0].device)
+        out["chain_us_per_layer_no_overlap"] = round(time_chain(chain, stream), 4)
+        mx.set_programmatic_launch(3)
+        out["chain_us_per_layer"] = round(time_chain(chain, stream), 4)
+        out["chain_layers"] = len(chain.layers)
+        out["chain_how"] = (f"a CUDA graph of {len(chain.layers)} dependent layers alternating [M,K]->[M,N] and "
+                            f"[M,N]->[M,K], each with its own weight copy; µs per layer")
+        del chain
+    finally:
+        mx.set_programmatic_launch(3)
+    return out
+
+
 def run_ours(args) -> dict:
     import block_scaled_mxfp4_activation_gb300 as mx
 
@@ -363,12 +472,13 @@ def run_ours(args) -> dict:
         dist.init_process_group("gloo")
         barrier = dist.barrier
     mx.load_library()
+    mx.set_programmatic_launch(3)
     peaks = measured_peaks()
     stream = torch.cuda.Stream(device)
     warmup = max(args.warmup, 3)
 
     name = args.workload
-    w = workloads.WORKLOADS[name]
+    w = ALL_WORKLOADS[name]
     prob = Problem(w, device)
     plan = mx.gemm_plan(w.M, w.N, w.K, fused=True)
     assert mx.device_error(reset=True) == 0
@@ -377,7 +487,6 @@ def run_ours(args) -> dict:
         ms = time_graph_steps(prob, args.steps, warmup, stream, barrier=barrier)
     clocks = clk.summary()
     ms_total, value = aggregate_over_ranks(ms, args.steps, world)
-    us_call = ms_total * 1e3 / args.steps
 
     ms_warm = time_graph_steps(prob, min(args.steps, 2000), warmup, stream, rotate=False)
     us_warm = ms_warm * 1e3 / min(args.steps, 2000)
@@ -390,6 +499,7 @@ def run_ours(args) -> dict:
     if err:
         raise RuntimeError(f"device error word {err:#x} after timing")
 
+    us_call = ms_total * 1e3 / args.steps
     rep = shape_report(name, us_call, peaks)
     traffic = committed_traffic(name)
     out = {
@@ -398,12 +508,13 @@ def run_ours(args) -> dict:
         "scaling": "weak", "vs_baseline": round(value / PAGES_US[name], 4) if name in PAGES_US else None,
         "vs_baseline_note": "pages' figure is end-to-end per call on MI355X incl. Python dispatch (context)",
         "dtype": "mxfp4", "data": "synthetic",
-        "config": {"workload": f"{name}: fused bf16->MXFP4 quantize + block-scaled GEMM, {w.label}",
-                   "M": w.M, "N": w.N, "K": w.K, "seed": w.seed,
-                   "l2": f"{prob.copies} rotating copies of A and packed B ({prob.rotating_bytes / 2**20:.0f} MiB "
-                         f"> 2x L2 {prob.l2 / 2**20:.0f} MiB)",
-                   "timing": "CUDA graph of calls replayed, CUDA events on the replay stream",
-                   "plan": plan},
+        "config": bench_config(w),
+        "timing": {"how": "a CUDA graph of calls replayed until exactly `steps` calls ran, CUDA events on the "
+                          "replay stream; call i on rotating copy i of A and of the packed weight; programmatic "
+                          "launch mode 3 (each call overlaps the one before it)",
+                   "copies": prob.copies, "rotating_mib": round(prob.rotating_bytes / 2**20, 1),
+                   "l2_mib": round(prob.l2 / 2**20, 1)},
+        "plan": plan,
         "roofline": {"bound": "hbm", "achieved": rep["gbs"], "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": rep["hbm_frac"], "traffic": traffic,
                      "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs)" if peaks["source"] == "measured"
@@ -421,17 +532,20 @@ def run_ours(args) -> dict:
                 "python_prepared_value": round(us_e2e_prep, 3),
                 "python_prepared_how": "the same step through prepare_quant_gemm_host (arguments checked once, then "
                                        "one call per step)"},
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * prob.launches_per_call,
         "clocks": clocks,
     }
     if args.all_shapes:
         shapes = {}
-        for other in workloads.WORKLOADS:
-            wo = workloads.WORKLOADS[other]
+        names = list(workloads.WORKLOADS) + list(workloads.EXTRA_WORKLOADS)
+        for other in names:
+            wo = ALL_WORKLOADS[other]
             p = prob if other == name else Problem(wo, device)
             n = min(max(args.steps, 1000), 4000)
             t = time_graph_steps(p, n, warmup, stream)
             r = shape_report(other, t * 1e3 / n, peaks)
+            if other in workloads.WORKLOADS:
+                r.update(latency_report(wo, p, stream, warmup, n))
             r["plan"] = mx.gemm_plan(wo.M, wo.N, wo.K, fused=True)
             r["pages_us_mi355x"] = PAGES_US.get(other)
             shapes[other] = r
@@ -439,6 +553,12 @@ def run_ours(args) -> dict:
                 del p
                 torch.cuda.empty_cache()
         out["per_shape"] = shapes
+        head = shapes[name]
+        out["latency"] = {k: head[k] for k in ("us_per_call_no_overlap", "chain_us_per_layer",
+                                               "chain_us_per_layer_no_overlap") if k in head}
+        err = mx.device_error(reset=True)
+        if err:
+            raise RuntimeError(f"device error word {err:#x} after the per-shape timings")
     if rank == 0 and world == 1 and not args.no_cpu:
         out["cpu_baseline"] = cpu_baseline(name)
         # all host cores, each process on half as many elements as the one-core run summed
@@ -461,7 +581,7 @@ def run_reference(args) -> dict | None:
 
     oracle.build()
     name = args.workload
-    w = workloads.WORKLOADS[name]
+    w = ALL_WORKLOADS[name]
     A, B = workloads.make_inputs(w)
     bq, bs = oracle.quantize(B)
     warmup = max(args.warmup, 3)
@@ -491,8 +611,7 @@ def run_reference(args) -> dict | None:
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": 1,
         "steps": args.steps, "warmup": warmup, "ms_per_step": round(us / 1e3, 4), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{name}: fused bf16->MXFP4 quantize + GEMM, {w.label}", "M": w.M, "N": w.N,
-                   "K": w.K, "seed": w.seed},
+        "config": bench_config(w),
         "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
@@ -505,7 +624,7 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=20000)
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(workloads.WORKLOADS))
+    ap.add_argument("--workload", default=workloads.HEADLINE, choices=sorted(ALL_WORKLOADS))
     ap.add_argument("--all-shapes", dest="all_shapes", action="store_true", default=True)
     ap.add_argument("--headline-only", dest="all_shapes", action="store_false")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

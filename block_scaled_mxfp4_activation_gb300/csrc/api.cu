@@ -196,22 +196,21 @@ size_t two_pass_workspace(int64_t M, int64_t K) {
          align256(static_cast<size_t>(M) * static_cast<size_t>(K / 32));
 }
 
-constexpr int64_t kMaxDim = int64_t(1) << 30;
 
-mxfp4_status_t check_mnk(int64_t M, int64_t N, int64_t K) {
-  if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MXFP4_ERR_INVALID_ARG;
-  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-  // 32-bit indices inside the kernels
-  if (M * N > (int64_t(1) << 31) || K / 2 * ceil_div(N, kTileN) * kTileN > (int64_t(1) << 40))
-    return MXFP4_ERR_UNSUPPORTED_SHAPE;
-  return MXFP4_OK;
-}
+// One GEMM launch with every argument checked, its plan chosen and its tensor
+// maps encoded: everything that can fail before anything is enqueued.
+struct PreparedGemm {
+  CUtensorMap map, amap, cmap;
+  GemmArgs g;
+  mxfp4_plan_t plan;
+  bool fused;
+};
 
 // c_host: null, or the device address of a second [M, N] output in mapped
 // host memory that the kernel writes alongside C.
-mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* bpacked, void* C,
-                        int64_t M, int64_t N, int64_t K, bool fused, const mxfp4_plan_t* user_plan,
-                        cudaStream_t stream, void* c_host = nullptr) {
+mxfp4_status_t prepare_gemm(const void* a, int64_t lda, const void* as, const void* bpacked, void* C, int64_t M,
+                            int64_t N, int64_t K, bool fused, const mxfp4_plan_t* user_plan, void* c_host,
+                            PreparedGemm* out) {
   mxfp4_status_t st = check_mnk(M, N, K);
   if (st != MXFP4_OK) return st;
   if (a == nullptr || bpacked == nullptr || C == nullptr || (!fused && as == nullptr))
@@ -219,10 +218,9 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   if (fused && lda < K) return MXFP4_ERR_INVALID_ARG;
   if (!aligned16(a) || !aligned16(bpacked) || !aligned16(C) || (fused && lda % 8 != 0))
     return MXFP4_ERR_MISALIGNED;
-  if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   const DeviceInfo* dev = current_device(&st);
   if (dev == nullptr) return st;
-  mxfp4_plan_t plan;
+  mxfp4_plan_t& plan = out->plan;
   if (user_plan != nullptr) {
     plan = mxfp4_plan_t{};
     plan.block_m = user_plan->block_m;
@@ -234,14 +232,15 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
     cached_default_plan(M, N, K, fused, dev->prop, &plan);
     if (plan.threads == 0) return MXFP4_ERR_UNSUPPORTED_SHAPE;
   }
-  CUtensorMap map, amap, cmap;
-  if (!encode_weight_map(bpacked, N, K, &map)) return failure("cuTensorMapEncodeTiled (weights)");
-  if (!encode_activation_map(a, M, K, fused ? lda : K / 2, fused, plan.block_m, &amap))
+  out->fused = fused;
+  if (!encode_weight_map(bpacked, N, K, &out->map)) return failure("cuTensorMapEncodeTiled (weights)");
+  if (!encode_activation_map(a, M, K, fused ? lda : K / 2, fused, plan.block_m, &out->amap))
     return failure("cuTensorMapEncodeTiled (activation)");
   // without a K split the output tile leaves by TMA store when a map can describe C
-  memset(&cmap, 0, sizeof(cmap));
-  const bool c_tma = plan.splits == 1 && encode_output_map(C, M, N, plan.block_m, &cmap);
-  GemmArgs g{};
+  memset(&out->cmap, 0, sizeof(out->cmap));
+  const bool c_tma = plan.splits == 1 && encode_output_map(C, M, N, plan.block_m, &out->cmap);
+  GemmArgs& g = out->g;
+  g = GemmArgs{};
   g.a = a;
   g.a_scales = static_cast<const uint8_t*>(as);
   const PackedLayout L = packed_layout(N, K);
@@ -274,35 +273,112 @@ mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* 
   g.trigger_late = g_programmatic.load() >= 3 ? 1 : 0;
   g.err = device_error_word();
   if (g.err == nullptr) return failure("cudaGetSymbolAddress (device error word)");
-  const cudaError_t e = launch_gemm(map, amap, cmap, g, plan, fused, g_programmatic.load() != 0, stream);
+  return MXFP4_OK;
+}
+
+mxfp4_status_t launch_prepared(const PreparedGemm& p, cudaStream_t stream) {
+  const cudaError_t e = launch_gemm(p.map, p.amap, p.cmap, p.g, p.plan, p.fused, g_programmatic.load() != 0, stream);
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("GEMM launch", e);
 }
 
-// mxfp4_quant_gemm, with the optional host copy of C (see run_gemm).
-mxfp4_status_t quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M, int64_t N,
-                          int64_t K, void* ws, size_t ws_bytes, cudaStream_t s, void* c_host) {
+mxfp4_status_t run_gemm(const void* a, int64_t lda, const void* as, const void* bpacked, void* C, int64_t M,
+                        int64_t N, int64_t K, bool fused, const mxfp4_plan_t* user_plan, cudaStream_t stream,
+                        void* c_host = nullptr) {
+  PreparedGemm p;
+  const mxfp4_status_t st = prepare_gemm(a, lda, as, bpacked, C, M, N, K, fused, user_plan, c_host, &p);
+  return st != MXFP4_OK ? st : launch_prepared(p, stream);
+}
+
+// The checks of mxfp4_quantize that need no device.
+mxfp4_status_t check_quantize_args(const void* A, int64_t M, int64_t K, int64_t lda, const void* Aq,
+                                   const void* As) {
+  if (A == nullptr || Aq == nullptr || As == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (M < 1 || K < 32 || K % 32 != 0 || lda < K) return MXFP4_ERR_INVALID_ARG;
+  if (M > kMaxDim || K > kMaxDim || M * (K / 16) > (int64_t(1) << 31) * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (!aligned16(A) || !aligned16(Aq) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  return MXFP4_OK;
+}
+
+// The fused layer, prepared: the GEMM launch and, on the two-pass route, the
+// quantize pass in front of it.
+struct PreparedQuantGemm {
+  PreparedGemm gemm;
+  bool two_pass = false;
+  const void* A = nullptr;
+  int64_t lda = 0, M = 0, K = 0;
+  void *Aq = nullptr, *As = nullptr;
+};
+
+// Every check of the fused entry (and of both launches of its two-pass route),
+// nothing enqueued.
+mxfp4_status_t prepare_quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M, int64_t N,
+                                  int64_t K, void* ws, size_t ws_bytes, void* c_host, PreparedQuantGemm* q) {
   mxfp4_status_t st = check_mnk(M, N, K);
   if (st != MXFP4_OK) return st;
-  if (two_pass_wanted(M) && ws != nullptr && ws_bytes >= two_pass_workspace(M, K) && aligned16(ws)) {
-    // validate everything the GEMM checks before anything is launched
-    if (A == nullptr || Bpacked == nullptr || C == nullptr) return MXFP4_ERR_INVALID_ARG;
-    if (lda < K) return MXFP4_ERR_INVALID_ARG;
-    if (!aligned16(A) || !aligned16(Bpacked) || !aligned16(C) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
-    if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-    // Two passes: quantize A once into the workspace, then the GEMM on codes
-    // (the fused kernel would re-read the 4x larger bf16 A in every N tile).
-    uint8_t* Aq = static_cast<uint8_t*>(ws);
-    uint8_t* As = Aq + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
-    st = mxfp4_quantize(A, M, K, lda, Aq, As, s);
-    if (st != MXFP4_OK) return st;
-    return run_gemm(Aq, K / 2, As, Bpacked, C, M, N, K, false, nullptr, s, c_host);
+  if (ws_bytes > 0 && ws == nullptr) return MXFP4_ERR_INVALID_ARG;
+  q->two_pass = ws_bytes > 0 && two_pass_wanted(M);
+  if (!q->two_pass) return prepare_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, c_host, &q->gemm);
+  if (ws_bytes < two_pass_workspace(M, K)) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+  if (!aligned16(ws)) return MXFP4_ERR_MISALIGNED;
+  q->A = A;
+  q->lda = lda;
+  q->M = M;
+  q->K = K;
+  q->Aq = ws;
+  q->As = static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
+  st = check_quantize_args(A, M, K, lda, q->Aq, q->As);
+  if (st != MXFP4_OK) return st;
+  return prepare_gemm(q->Aq, K / 2, q->As, Bpacked, C, M, N, K, false, nullptr, c_host, &q->gemm);
+}
+
+mxfp4_status_t launch_quant_gemm(const PreparedQuantGemm& q, cudaStream_t s) {
+  if (q.two_pass) {
+    const cudaError_t e = launch_quantize(q.A, q.M, q.K, q.lda, q.Aq, q.As, g_programmatic.load() != 0, s);
+    if (e != cudaSuccess) return cuda_failure("quantize launch", e);
   }
-  return run_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, s, c_host);
+  return launch_prepared(q.gemm, s);
 }
 
 }  // namespace
 
 void set_last_error(const char* what) { snprintf(g_last_error, sizeof(g_last_error), "%s", what); }
+
+mxfp4_status_t check_mnk(int64_t M, int64_t N, int64_t K) {
+  if (M < 1 || N < 1 || K < 32 || K % 32 != 0) return MXFP4_ERR_INVALID_ARG;
+  if (M > kMaxDim || N > kMaxDim || K > kMaxDim) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  // 32-bit indices and grid limits inside the kernels
+  if (M * N > (int64_t(1) << 31) || K / 2 * ceil_div(N, kTileN) * kTileN > (int64_t(1) << 40) ||
+      M > 65535LL * 256)
+    return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  return MXFP4_OK;
+}
+
+mxfp4_status_t check_device() {
+  mxfp4_status_t st;
+  current_device(&st);
+  return st;
+}
+
+mxfp4_status_t two_pass(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M, int64_t N, int64_t K,
+                        void* Aq, void* As, cudaStream_t s, void* c_host) {
+  // Every check of both launches first (the GEMM's plan and tensor maps
+  // included), so that an error status means nothing was launched.
+  mxfp4_status_t st = check_mnk(M, N, K);
+  if (st != MXFP4_OK) return st;
+  PreparedQuantGemm q;
+  q.two_pass = true;
+  q.A = A;
+  q.lda = lda;
+  q.M = M;
+  q.K = K;
+  q.Aq = Aq;
+  q.As = As;
+  st = check_quantize_args(A, M, K, lda, Aq, As);
+  if (st != MXFP4_OK) return st;
+  st = prepare_gemm(Aq, K / 2, As, Bpacked, C, M, N, K, false, nullptr, c_host, &q.gemm);
+  if (st != MXFP4_OK) return st;
+  return launch_quant_gemm(q, s);
+}
 
 }  // namespace mxfp4
 
@@ -312,11 +388,8 @@ extern "C" {
 
 mxfp4_status_t mxfp4_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
                               mxfp4_stream_t stream) {
-  if (A == nullptr || Aq == nullptr || As == nullptr) return MXFP4_ERR_INVALID_ARG;
-  if (M < 1 || K < 32 || K % 32 != 0 || lda < K) return MXFP4_ERR_INVALID_ARG;
-  if (M > kMaxDim || K > kMaxDim || M * (K / 16) > (int64_t(1) << 31) * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
-  if (!aligned16(A) || !aligned16(Aq) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
-  mxfp4_status_t st;
+  mxfp4_status_t st = check_quantize_args(A, M, K, lda, Aq, As);
+  if (st != MXFP4_OK) return st;
   if (current_device(&st) == nullptr) return st;
   const cudaError_t e =
       launch_quantize(A, M, K, lda, Aq, As, g_programmatic.load() != 0, reinterpret_cast<cudaStream_t>(stream));
@@ -379,7 +452,9 @@ mxfp4_status_t mxfp4_gemm(const void* Aq, const void* As, const void* Bpacked, v
 
 mxfp4_status_t mxfp4_quant_gemm(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M,
                                 int64_t N, int64_t K, void* ws, size_t ws_bytes, mxfp4_stream_t stream) {
-  return quant_gemm(A, lda, Bpacked, C, M, N, K, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), nullptr);
+  PreparedQuantGemm q;
+  const mxfp4_status_t st = prepare_quant_gemm(A, lda, Bpacked, C, M, N, K, ws, ws_bytes, nullptr, &q);
+  return st != MXFP4_OK ? st : launch_quant_gemm(q, reinterpret_cast<cudaStream_t>(stream));
 }
 
 mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void* A_dev, int64_t lda_dev,
@@ -388,13 +463,17 @@ mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void*
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   mxfp4_status_t st = check_mnk(M, N, K);
   if (st != MXFP4_OK) return st;
-  // every check of mxfp4_quant_gemm first, so that an error launches nothing
-  if (A_host == nullptr || C_host == nullptr || A_dev == nullptr || Bpacked == nullptr || C_dev == nullptr)
-    return MXFP4_ERR_INVALID_ARG;
-  if (lda_host < K || lda_dev < K) return MXFP4_ERR_INVALID_ARG;
-  if (!aligned16(A_dev) || !aligned16(Bpacked) || !aligned16(C_dev) || lda_dev % 8 != 0)
-    return MXFP4_ERR_MISALIGNED;
-  if (M > 65535LL * 256) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  if (A_host == nullptr || C_host == nullptr || A_dev == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (lda_host < K) return MXFP4_ERR_INVALID_ARG;
+  // A mapped C_host is written by the GEMM kernel itself, beside C_dev (no
+  // download pass); any other by the copy engines afterwards.
+  void* c_dst = const_cast<void*>(device_view(C_host));
+  const bool c_direct = c_dst != nullptr && aligned16(c_dst);
+  // every check of the layer (both routes, plan and tensor maps included)
+  // before the upload, so that an error launches nothing
+  PreparedQuantGemm q;
+  st = prepare_quant_gemm(A_dev, lda_dev, Bpacked, C_dev, M, N, K, ws, ws_bytes, c_direct ? c_dst : nullptr, &q);
+  if (st != MXFP4_OK) return st;
   const DeviceInfo* dev = current_device(&st);
   if (dev == nullptr) return st;
   const bool programmatic = g_programmatic.load() != 0;
@@ -410,11 +489,7 @@ mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void*
                           static_cast<size_t>(K) * 2, static_cast<size_t>(M), cudaMemcpyHostToDevice, s);
   }
   if (e != cudaSuccess) return cuda_failure("activation upload", e);
-  // A mapped C_host is written by the GEMM kernel itself, beside C_dev (no
-  // download pass); any other by the copy engines afterwards.
-  void* c_dst = const_cast<void*>(device_view(C_host));
-  const bool c_direct = c_dst != nullptr && aligned16(c_dst);
-  st = quant_gemm(A_dev, lda_dev, Bpacked, C_dev, M, N, K, ws, ws_bytes, s, c_direct ? c_dst : nullptr);
+  st = launch_quant_gemm(q, s);
   if (st != MXFP4_OK || c_direct) return st;
   e = cudaMemcpyAsync(C_host, C_dev, static_cast<size_t>(M * N * 2), cudaMemcpyDeviceToHost, s);
   return e == cudaSuccess ? MXFP4_OK : cuda_failure("result download", e);

@@ -791,7 +791,7 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // split's K tiles).  Ties prefer the larger block_m (fewer re-reads of the
 // weights), then the larger stage count, then fewer splits.
 // Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
-// the estimate is not: sweeps of block_m x splits x stages, graph-replayed
+// the estimate is not (keyed on the shape): sweeps of block_m x splits x stages, graph-replayed
 // calls with rotating operands.  `fused` is the GEMM kernel's kind (the large-M
 // shapes run the pre-quantized kernel on the fused entry's two-pass route).
 struct TunedPlan {
@@ -815,17 +815,20 @@ static int64_t plan_cost_ns(const mxfp4_plan_t& p, int64_t M, bool fused) {
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
                   mxfp4_plan_t* p) {
   *p = mxfp4_plan_t{};
-  if (prop.multiProcessorCount == 152) {
-    for (const TunedPlan& t : kTunedPlans) {
-      if (t.M != M || t.N != N || t.K != K || t.fused != fused) continue;
-      mxfp4_plan_t q{};
-      q.block_m = t.block_m;
-      q.splits = t.splits;
-      q.stages = t.stages;
-      if (finish_plan(M, N, K, fused, prop, &q)) {
-        *p = q;
-        return;
-      }
+  // A tuned plan is keyed on the shape; it is taken on any device where it
+  // still fits and runs in one wave (every cluster resident at once).
+  for (const TunedPlan& t : kTunedPlans) {
+    if (t.M != M || t.N != N || t.K != K || t.fused != fused) continue;
+    mxfp4_plan_t q{};
+    q.block_m = t.block_m;
+    q.splits = t.splits;
+    q.stages = t.stages;
+    if (!finish_plan(M, N, K, fused, prop, &q)) continue;
+    const int64_t clusters = static_cast<int64_t>(q.grid_y) * q.grid_z;
+    if (clusters * q.splits <= 2 * static_cast<int64_t>(prop.multiProcessorCount) &&
+        clusters <= active_clusters(q, fused)) {
+      *p = q;
+      return;
     }
   }
   const int bm0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;

@@ -22,6 +22,9 @@ constexpr int kMaxSplits = 8;                    // portable cluster size
 
 inline int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Largest M, N or K any entry accepts.
+constexpr int64_t kMaxDim = int64_t(1) << 30;
+
 struct PackedLayout {
   int64_t n_pad;     // rows rounded up to kTileN
   int64_t k_tiles;   // ceil(K / kTileK)
@@ -116,6 +119,19 @@ cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, co
                         cudaStream_t s);
 
 cudaError_t read_device_error(cudaStream_t s, uint32_t* code, bool reset);
+// The size checks every GEMM entry makes: MXFP4_ERR_INVALID_ARG for
+// non-positive sizes or K % 32 != 0, MXFP4_ERR_UNSUPPORTED_SHAPE past the
+// kernels' index and grid limits.
+mxfp4_status_t check_mnk(int64_t M, int64_t N, int64_t K);
+// MXFP4_OK if the current device is an sm_103 GPU, else the status every
+// entry returns for it (MXFP4_ERR_UNSUPPORTED_DEVICE or MXFP4_ERR_CUDA).
+mxfp4_status_t check_device();
+// The fused layer's two-pass route: A quantized into Aq [M, K/2] and As
+// [M, K/32] (caller-owned scratch), then the GEMM on the codes.  Every check
+// of both launches (device, plan, tensor maps) comes before the first launch;
+// an error status means nothing was enqueued.  c_host as for the host entry.
+mxfp4_status_t two_pass(const void* A, int64_t lda, const void* Bpacked, void* C, int64_t M, int64_t N, int64_t K,
+                        void* Aq, void* As, cudaStream_t s, void* c_host);
 // Sets the calling thread's message for mxfp4_last_error_string().
 void set_last_error(const char* what);
 // Address of the device error word on the current device (nullptr on failure).

@@ -55,13 +55,13 @@ using namespace mxfp4;
 extern "C" mxfp4_status_t mxfp4_quant_gemm_static_scratch(const void* A, int64_t lda, const void* Bpacked,
                                                           void* C, int64_t M, int64_t N, int64_t K,
                                                           mxfp4_stream_t stream) {
-  // Every check that the two launches below make, made first: a call that
-  // returns an error has launched nothing.
-  if (A == nullptr || Bpacked == nullptr || C == nullptr) return MXFP4_ERR_INVALID_ARG;
-  if (M < 1 || N < 1 || K < 32 || K % 32 != 0 || lda < K) return MXFP4_ERR_INVALID_ARG;
-  const int64_t kMax = int64_t(1) << 30;
-  if (M > kMax || N > kMax || K > kMax || M * N > (int64_t(1) << 31) || M > 65535LL * 256)
-    return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  // The size limits of the GEMM entries, then this entry's own limit, then
+  // pointers, the device and the array's address; two_pass() makes every
+  // remaining check of both launches (plan and tensor maps included) before
+  // the first one, so a call that returns an error has launched nothing.
+  mxfp4_status_t st = check_mnk(M, N, K);
+  if (st != MXFP4_OK) return st;
+  if (A == nullptr || Bpacked == nullptr || C == nullptr || lda < K) return MXFP4_ERR_INVALID_ARG;
   const size_t codes = round256(static_cast<size_t>(M) * static_cast<size_t>(K / 2));
   const size_t need = codes + round256(static_cast<size_t>(M) * static_cast<size_t>(K / 32));
   if (need > kStaticScratchBytes) {
@@ -71,6 +71,8 @@ extern "C" mxfp4_status_t mxfp4_quant_gemm_static_scratch(const void* A, int64_t
   const uintptr_t mis = reinterpret_cast<uintptr_t>(A) | reinterpret_cast<uintptr_t>(Bpacked) |
                         reinterpret_cast<uintptr_t>(C);
   if ((mis & 15u) != 0 || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  st = check_device();
+  if (st != MXFP4_OK) return st;
   cudaError_t e;
   uint8_t* scratch = static_scratch_address(&e);
   if (scratch == nullptr) {
@@ -79,7 +81,6 @@ extern "C" mxfp4_status_t mxfp4_quant_gemm_static_scratch(const void* A, int64_t
   }
   // Quantization overwrites every byte the GEMM then reads, so nothing needs
   // clearing between calls.
-  mxfp4_status_t st = mxfp4_quantize(A, M, K, lda, scratch, scratch + codes, stream);
-  if (st != MXFP4_OK) return st;
-  return mxfp4_gemm(scratch, scratch + codes, Bpacked, C, M, N, K, nullptr, 0, stream);
+  return two_pass(A, lda, Bpacked, C, M, N, K, scratch, scratch + codes, reinterpret_cast<cudaStream_t>(stream),
+                  nullptr);
 }

@@ -26,6 +26,10 @@
  *   - Device-side waits are bounded (about one second by default).  A wait
  *     that runs out sets the library's device error word and the kernel
  *     finishes without its result; read the word with mxfp4_device_error().
+ *   - The library keeps device arrays of its own (the error word, and the
+ *     scratch of mxfp4_quant_gemm_static_scratch) and resolves their device
+ *     addresses once per device.  A cudaDeviceReset() in the process
+ *     invalidates those addresses: do not call the library after one.
  */
 #ifndef MXFP4_H_
 #define MXFP4_H_
@@ -45,7 +49,7 @@ typedef enum {
   MXFP4_ERR_INVALID_ARG = 1,        /* null pointer, non-positive size, K % 32 != 0, bad plan */
   MXFP4_ERR_UNSUPPORTED_SHAPE = 2,  /* a size beyond the library's limits */
   MXFP4_ERR_MISALIGNED = 3,         /* a pointer or leading dimension not 16-byte aligned */
-  MXFP4_ERR_WORKSPACE_TOO_SMALL = 4,
+  MXFP4_ERR_WORKSPACE_TOO_SMALL = 4,/* a workspace smaller than the chosen route needs */
   MXFP4_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
   MXFP4_ERR_DEVICE_TIMEOUT = 6,     /* a device-side bounded wait ran out */
   MXFP4_ERR_UNSUPPORTED_DEVICE = 7  /* the current device is not sm_103 */
@@ -135,14 +139,22 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
  *   Bpacked  device, the output of mxfp4_pack_weights for the same N, K
  *   C        device, bf16 [M, N] row-major, fully overwritten
  *   ws, ws_bytes  device scratch, optional (NULL, 0 is always valid).
- *            mxfp4_gemm never uses it.  mxfp4_quant_gemm uses it when M >= 64
- *            and ws_bytes >= mxfp4_workspace_bytes(M, N, K) (16-byte aligned):
- *            it then quantizes A into the workspace with mxfp4_quantize and
- *            runs the GEMM on the codes -- two launches that overlap, and
- *            faster than the single fused kernel once M is large, because the
- *            fused kernel re-reads the bf16 activation in every 128-row weight
- *            tile.  Without it, the single fused kernel runs.  The workspace
- *            is overwritten; calls that share one must be ordered.
+ *            mxfp4_gemm needs none: it accepts and ignores any ws, ws_bytes.
+ *            mxfp4_quant_gemm chooses its route by them:
+ *              - ws_bytes == 0: the single fused kernel, for every M;
+ *              - ws_bytes > 0 and M >= 64 (where mxfp4_workspace_bytes() is
+ *                non-zero): the two-pass route -- A quantized into the
+ *                workspace by mxfp4_quantize, then the GEMM on the codes, two
+ *                launches that overlap; faster than the single kernel once M
+ *                is large, because that kernel re-reads the bf16 activation
+ *                in every 128-row weight tile.  ws_bytes below
+ *                mxfp4_workspace_bytes(M, N, K) returns
+ *                MXFP4_ERR_WORKSPACE_TOO_SMALL, a ws that is not 16-byte
+ *                aligned MXFP4_ERR_MISALIGNED (nothing launched);
+ *              - ws_bytes > 0 and M < 64: the single fused kernel (ws unused);
+ *              - ws == NULL with ws_bytes > 0: MXFP4_ERR_INVALID_ARG.
+ *            The workspace is overwritten; calls that share one must be
+ *            ordered.
  * M, N >= 1.  Returns MXFP4_OK or an error status (nothing launched).
  * ------------------------------------------------------------------------- */
 /* Workspace that lets mxfp4_quant_gemm take its two-pass route (0 when the
@@ -226,8 +238,11 @@ mxfp4_status_t mxfp4_gemm_with_plan(const void* A_or_Aq, int64_t lda, const void
  * ------------------------------------------------------------------------- */
 const char* mxfp4_status_string(mxfp4_status_t status);
 
-/* The CUDA call and error behind the last MXFP4_ERR_CUDA status returned on
- * the calling thread ("" if none); valid until the thread's next call. */
+/* A message for the last MXFP4_ERR_CUDA status returned on the calling
+ * thread (the CUDA call and its error), or for the last
+ * MXFP4_ERR_UNSUPPORTED_SHAPE that mxfp4_quant_gemm_static_scratch returned
+ * because its size limit was exceeded; "" if none.  Valid until the thread's
+ * next call that sets it. */
 const char* mxfp4_last_error_string(void);
 
 /* Synchronises `stream`, then reads the device error word (0 = no device-side

@@ -97,6 +97,37 @@ def test_argument_checks_launch_nothing(lib):
     assert lib.mxfp4_pack_weights_shuffled(fake, fake, 32, 128, odd, None) == MISALIGNED
     assert lib.mxfp4_gemm_plan(4, 128, 64, 1, None) == INVALID
     assert lib.mxfp4_device_error(None, 0, None) == INVALID
+    # the fused entry's workspace: offered but too small for the two-pass route
+    # (M >= 64), offered as a null pointer, or misaligned
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 64, 128, 64, fake, 16, None) == WS_SMALL
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 64, 128, 64, None, 1 << 20, None) == INVALID
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 64, 128, 64, odd, 1 << 20, None) == MISALIGNED
+    assert lib.mxfp4_quant_gemm_host(fake, 64, fake, 64, fake, fake, fake, 64, 128, 64, fake, 16, None) == WS_SMALL
+
+
+def test_static_scratch_entry_checks_launch_nothing(lib):
+    fake = ctypes.c_void_p(0x10000)  # never dereferenced: checks fail first
+    odd = ctypes.c_void_p(0x10001)
+    fn = lib.mxfp4_quant_gemm_static_scratch
+    fn.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+                   ctypes.c_int64, ctypes.c_int64, ctypes.c_void_p]
+    fn.restype = ctypes.c_int
+    lib.mxfp4_last_error_string.restype = ctypes.c_char_p
+    assert fn(fake, 64, fake, None, 4, 128, 64, None) == INVALID  # null C
+    assert fn(None, 64, fake, fake, 4, 128, 64, None) == INVALID  # null A
+    assert fn(fake, 32, fake, fake, 4, 128, 64, None) == INVALID  # lda < K
+    assert fn(fake, 48, fake, fake, 4, 128, 48, None) == INVALID  # K % 32
+    assert fn(fake, 64, fake, fake, 0, 128, 64, None) == INVALID
+    assert fn(odd, 64, fake, fake, 4, 128, 64, None) == MISALIGNED
+    assert fn(fake, 64, odd, fake, 4, 128, 64, None) == MISALIGNED
+    assert fn(fake, 64, fake, odd, 4, 128, 64, None) == MISALIGNED
+    assert fn(fake, 68, fake, fake, 4, 128, 64, None) == MISALIGNED  # lda % 8
+    # the kernels' index limits, with an activation that fits the 4 MiB scratch
+    assert fn(fake, 64, fake, fake, 1 << 11, 1 << 21, 64, None) == UNSUPPORTED  # M * N > 2^31
+    assert fn(fake, 1 << 22, fake, fake, 1, 1 << 20, 1 << 22, None) == UNSUPPORTED  # K/2 * N > 2^40
+    # the scratch limit itself, named by the error string
+    assert fn(fake, 8192, fake, fake, 4096, 128, 8192, None) == UNSUPPORTED
+    assert b"4 MiB" in lib.mxfp4_last_error_string()
 
 
 def test_python_binding_refuses_cpu_tensors():

@@ -391,3 +391,16 @@ def test_workload_recipe_shapes():
     A, _ = workloads.make_inputs("m16_n2112_k7168")
     frac = (A.float().abs() > 20).float().mean().item()
     assert 0.005 < frac < 0.015  # about 1% outliers
+
+
+def test_blocked_full_gemm_equals_one_call(oracle_mod):
+    """The parallel block-wise oracle GEMM used by the full-size GPU tests gives
+    exactly the single call's sums (each element is the same k-ordered sum)."""
+    from oracle_blocks import gemm_full
+
+    for M, N, K, threads in ((3, 50, 64, 4), (40, 7, 96, 3), (1, 300, 32, 8), (33, 65, 160, 5)):
+        A, B = workloads.make_random(M, N, K, seed=M + N + K)
+        aq, as_ = oracle_mod.quantize(A)
+        bq, bs = oracle_mod.quantize(B)
+        c1, _ = oracle_mod.gemm(aq, as_, bq, bs)
+        assert np.array_equal(gemm_full(oracle_mod, aq, as_, bq, bs, threads=threads), c1)
