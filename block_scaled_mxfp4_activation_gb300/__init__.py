@@ -25,7 +25,8 @@ __all__ = [
     "pack_weights", "pack_weights_shuffled", "unpack_weights", "quantize_weights", "gemm", "quant_gemm", "gemm_plan",
     "gemm_with_plan", "workspace_bytes", "device_error", "set_wait_timeout_ns", "diag_wait_timeout",
     "status_string", "Plan", "set_programmatic_launch", "custom_kernel", "quant_gemm_host",
-    "PreparedCall", "prepare_quant_gemm", "prepare_quant_gemm_host",
+    "PreparedCall", "prepare_quant_gemm", "prepare_quant_gemm_host", "chain_workspace_bytes", "quant_gemm_chain",
+    "chain_plan", "prepare_quant_gemm_chain",
 ]
 
 MXFP4_OK = 0
@@ -91,6 +92,11 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
             "mxfp4_set_programmatic_launch": ([ctypes.c_int], st),
             "mxfp4_last_error_string": ([], ctypes.c_char_p),
             "mxfp4_quant_gemm_host": ([P, I, P, I, P, P, P, I, I, I, P, Z, S], st),
+            "mxfp4_chain_workspace_bytes": ([I, I, ctypes.c_int32, ctypes.POINTER(I)], Z),
+            "mxfp4_quant_gemm_chain": ([P, I, I, I, ctypes.c_int32, ctypes.POINTER(P), ctypes.POINTER(I),
+                                        ctypes.POINTER(P), P, Z, S], st),
+            "mxfp4_chain_plan": ([I, I, ctypes.c_int32, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_int32),
+                                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], st),
         }
         for name, (args, res) in sig.items():
             fn = getattr(lib, name)
@@ -344,6 +350,72 @@ def prepare_quant_gemm_host(A_host: torch.Tensor, W: PackedWeight, A_dev: torch.
     delivers C to C_dev and C_host, returning C_host."""
     args = _quant_gemm_host_args(A_host, W, A_dev, C_dev, C_host, workspace, stream)
     return PreparedCall("mxfp4_quant_gemm_host", args, (A_host, W, A_dev, C_dev, C_host, workspace), C_host)
+
+
+# ----------------------------------------------------------------------------- several layers, one launch
+def chain_workspace_bytes(M: int, K: int, Ns) -> int:
+    """Workspace of quant_gemm_chain for activations [M, K] through layers of widths Ns."""
+    arr = (ctypes.c_int64 * len(Ns))(*[int(n) for n in Ns])
+    n = load_library().mxfp4_chain_workspace_bytes(int(M), int(K), len(Ns), arr)
+    if n == 0:
+        raise MXFP4Error(1, "mxfp4_chain_workspace_bytes")
+    return int(n)
+
+
+def chain_plan(M: int, K: int, Ns) -> dict:
+    """The multi-layer launch's plan: per-layer K splits, grid size, rows per CTA."""
+    L = len(Ns)
+    arr = (ctypes.c_int64 * L)(*[int(n) for n in Ns])
+    splits = (ctypes.c_int32 * L)()
+    grid, bm = ctypes.c_int32(0), ctypes.c_int32(0)
+    _call("mxfp4_chain_plan", int(M), int(K), L, arr, splits, ctypes.byref(grid), ctypes.byref(bm))
+    return {"splits": list(splits), "grid": grid.value, "block_m": bm.value}
+
+
+def _chain_args(A: torch.Tensor, weights, outs, workspace, stream) -> tuple:
+    _need(A, torch.bfloat16, "A")
+    if A.dim() != 2 or A.stride(1) != 1:
+        raise ValueError("A must be 2-D with unit column stride")
+    weights = [_weight(W) for W in weights]
+    M, K = A.shape
+    k = K
+    for W in weights:
+        if W.K != k:
+            raise ValueError("each layer's weight K must equal the previous layer's N (the first: A's K)")
+        k = W.N
+    Ns = [W.N for W in weights]
+    if outs is None:
+        outs = [torch.empty((M, n), dtype=torch.bfloat16, device=A.device) for n in Ns]
+    for o, n in zip(outs, Ns):
+        _need(o, torch.bfloat16, "out")
+        if o.shape != (M, n) or not o.is_contiguous():
+            raise ValueError("each output must be a contiguous [M, N_l] bf16 tensor")
+    if workspace is None:
+        workspace = torch.zeros(chain_workspace_bytes(M, K, Ns), dtype=torch.uint8, device=A.device)
+    L = len(weights)
+    b = (ctypes.c_void_p * L)(*[W.data.data_ptr() for W in weights])
+    n = (ctypes.c_int64 * L)(*Ns)
+    c = (ctypes.c_void_p * L)(*[o.data_ptr() for o in outs])
+    args = (A.data_ptr(), A.stride(0), M, K, L, b, n, c, workspace.data_ptr(), workspace.numel(), _stream(stream, A))
+    return args, outs, workspace, (b, n, c)
+
+
+def quant_gemm_chain(A: torch.Tensor, weights, outs=None, workspace: torch.Tensor | None = None,
+                     stream=None) -> list:
+    """Dependent layers in one launch: X_0 = A, C_l = quant(X_l) @ W_l^T, X_{l+1} = C_l.
+    Returns every layer's output.  `workspace` (uint8 CUDA tensor of at least
+    chain_workspace_bytes(M, K, Ns) bytes) must be zero-filled before its first
+    use; each call leaves it ready for the next (zero-filled here when None)."""
+    args, outs, _, _ = _chain_args(A, weights, outs, workspace, stream)
+    _call("mxfp4_quant_gemm_chain", *args)
+    return outs
+
+
+def prepare_quant_gemm_chain(A: torch.Tensor, weights, outs=None, workspace: torch.Tensor | None = None,
+                             stream=None) -> PreparedCall:
+    """quant_gemm_chain bound to these buffers (arguments checked once)."""
+    args, outs, workspace, keep = _chain_args(A, weights, outs, workspace, stream)
+    return PreparedCall("mxfp4_quant_gemm_chain", args, (A, list(weights), outs, workspace, keep), outs)
 
 
 def gemm_plan(M: int, N: int, K: int, fused: bool = True) -> dict:

@@ -15,8 +15,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libmxfp4.so")
-SOURCES = ["api.cu", "gemm.cu", "quantize.cu", "no_alloc.cu", "host_copy.cu"]
-HEADERS = ["internal.h", "ptx.cuh", "quant.cuh"]
+SOURCES = ["api.cu", "gemm.cu", "chain.cu", "quantize.cu", "no_alloc.cu", "host_copy.cu"]
+HEADERS = ["internal.h", "ptx.cuh", "quant.cuh", "tile.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--ptxas-options=-v", "-I", os.path.join(ROOT, "include")]

@@ -5,6 +5,7 @@
 #include <atomic>
 #include <cstdio>
 #include <cstring>
+#include <algorithm>
 #include <map>
 #include <mutex>
 #include <tuple>
@@ -99,7 +100,7 @@ bool encode_2d(CUtensorMapDataType type, const void* base, uint64_t dim0, uint64
     bool valid;
     CUtensorMap map;
   };
-  constexpr int kEntries = 16;
+  constexpr int kEntries = 64;  // room for a multi-layer launch's maps
   thread_local Entry cache[kEntries] = {};
   thread_local int next = 0;
   for (int i = 0; i < kEntries; ++i) {
@@ -339,6 +340,160 @@ mxfp4_status_t launch_quant_gemm(const PreparedQuantGemm& q, cudaStream_t s) {
   return launch_prepared(q.gemm, s);
 }
 
+// ----------------------------------------------------------------------------- multi-layer launch
+// Workspace of a multi-layer launch (every offset 256-aligned; independent of
+// the device, so the size can be queried without one): per layer the
+// activation codes [M, K_l/2] and scale chunks [m_tiles][k_tiles_l][1 KB],
+// split-K partials for up to min(8, k_tiles_l) splits, then every counter.
+struct ChainGeometry {
+  int bm = 0, m_tiles = 0, layers = 0;
+  struct Layer {
+    int64_t N, K;
+    int k_tiles, n_tiles, tiles, smax;
+    size_t codes, sf, part;
+    size_t done, tickets;  // counter indices
+  } layer[kMaxChainLayers];
+  size_t counters = 0, n_counters = 0, total = 0;
+};
+
+int chain_block_m(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+
+void chain_geometry(int64_t M, int64_t K, int L, const int64_t* N, ChainGeometry* g) {
+  g->bm = chain_block_m(M);
+  g->m_tiles = static_cast<int>(ceil_div(M, g->bm));
+  g->layers = L;
+  size_t off = 0, cnt = 0;
+  for (int l = 0; l < L; ++l) {
+    ChainGeometry::Layer& y = g->layer[l];
+    y.N = N[l];
+    y.K = l == 0 ? K : N[l - 1];
+    y.k_tiles = static_cast<int>(ceil_div(y.K, kTileK));
+    y.n_tiles = static_cast<int>(ceil_div(y.N, kTileN));
+    y.tiles = y.n_tiles * g->m_tiles;
+    y.smax = y.k_tiles < kMaxSplits ? y.k_tiles : kMaxSplits;
+    y.codes = off;
+    off += align256(static_cast<size_t>(M) * static_cast<size_t>(y.K / 2));
+    y.sf = off;
+    off += align256(static_cast<size_t>(g->m_tiles) * y.k_tiles * kSfTileBytes);
+    y.part = off;
+    if (y.smax > 1) off += align256(static_cast<size_t>(y.tiles) * y.smax * g->bm * kTileN * sizeof(float));
+    y.done = cnt;
+    cnt += static_cast<size_t>(g->m_tiles) * y.k_tiles;
+    y.tickets = cnt;
+    cnt += static_cast<size_t>(y.tiles);
+  }
+  g->counters = off;
+  g->n_counters = cnt + 1;  // + the exit counter
+  g->total = off + align256(g->n_counters * sizeof(uint32_t));
+}
+
+// The argument checks of a multi-layer launch that need no device.
+mxfp4_status_t check_chain_args(const void* A, int64_t lda, int64_t M, int64_t K, int32_t L,
+                                const void* const* Bpacked, const int64_t* N, void* const* C) {
+  if (L < 1 || L > kMaxChainLayers || Bpacked == nullptr || N == nullptr || C == nullptr || A == nullptr)
+    return MXFP4_ERR_INVALID_ARG;
+  if (lda < K) return MXFP4_ERR_INVALID_ARG;
+  for (int l = 0; l < L; ++l) {
+    const int64_t K_l = l == 0 ? K : N[l - 1];
+    mxfp4_status_t st = check_mnk(M, N[l], K_l);
+    if (st != MXFP4_OK) return st;
+    if (Bpacked[l] == nullptr || C[l] == nullptr) return MXFP4_ERR_INVALID_ARG;
+  }
+  if (!aligned16(A) || lda % 8 != 0) return MXFP4_ERR_MISALIGNED;
+  for (int l = 0; l < L; ++l)
+    if (!aligned16(Bpacked[l]) || !aligned16(C[l])) return MXFP4_ERR_MISALIGNED;
+  return MXFP4_OK;
+}
+
+struct ChainPlan {
+  int stages = 0, smem = 0, tmem_cols = 0, grid = 0;
+  int splits[kMaxChainLayers];
+};
+
+// Shared memory of one CTA of the multi-layer kernel, and its tensor-memory columns.
+void chain_smem(int bm, int stages, const cudaDeviceProp& prop, int* smem, int* tcols, uint32_t* offs) {
+  const uint32_t st = static_cast<uint32_t>(stages);
+  const uint32_t a_off = st * kTileN * kTileKBytes;
+  const uint32_t sfw_off = a_off + st * static_cast<uint32_t>(bm) * kTileKBytes;
+  const uint32_t sfa_off = sfw_off + st * kSfTileBytes;
+  const uint32_t bar_off = sfa_off + st * 2 * kSfChunkBytes;
+  const uint32_t total = bar_off + (3 * st + 2) * 8 + 16;
+  uint32_t t = 32;
+  while (t < static_cast<uint32_t>(bm + 16 * stages)) t <<= 1;
+  int64_t bytes = static_cast<int64_t>(total) + 1024;
+  // the same tensor-memory share rule as the single-layer kernel: CTAs that
+  // fit on an SM together never ask for more than its 512 columns
+  const int64_t floor_smem = (static_cast<int64_t>(prop.sharedMemPerMultiprocessor) * t + 511) / 512 -
+                             static_cast<int64_t>(prop.reservedSharedMemPerBlock);
+  if (bytes < floor_smem) bytes = floor_smem;
+  *smem = static_cast<int>((bytes + 15) / 16 * 16);
+  *tcols = static_cast<int>(t);
+  if (offs != nullptr) {
+    offs[0] = a_off;
+    offs[1] = sfw_off;
+    offs[2] = sfa_off;
+    offs[3] = bar_off;
+  }
+}
+
+// Stages (the deepest ring, up to 6, that still lets two CTAs share an SM),
+// then per layer the K split minimising an estimate of one item's critical
+// path (~250 ns per K tile in sequence, ~700 ns for the split-K sum) among
+// splits whose items all fit in one wave; the grid is the largest layer's
+// item count (at most one wave).
+bool chain_plan(const ChainGeometry& g, const cudaDeviceProp& prop, ChainPlan* pl) {
+  int stages = 6, smem = 0, tcols = 0;
+  for (; stages >= 2; --stages) {
+    chain_smem(g.bm, stages, prop, &smem, &tcols, nullptr);
+    if (2 * (static_cast<int64_t>(smem) + prop.reservedSharedMemPerBlock) <= prop.sharedMemPerMultiprocessor) break;
+  }
+  if (stages < 2) return false;
+  static std::mutex mu;
+  static std::map<std::tuple<int, int, int>, int> occ_cache;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  int per_sm = 0;
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto key = std::make_tuple(dev, g.bm, smem);
+    auto it = occ_cache.find(key);
+    if (it != occ_cache.end()) {
+      per_sm = it->second;
+    } else {
+      per_sm = chain_blocks_per_sm(g.bm, smem);
+      occ_cache[key] = per_sm;
+    }
+  }
+  if (per_sm < 1) return false;
+  const int cap = per_sm * prop.multiProcessorCount;
+  int grid = 1;
+  for (int l = 0; l < g.layers; ++l) {
+    const ChainGeometry::Layer& y = g.layer[l];
+    int best = 1;
+    int64_t best_cost = -1;
+    for (int S = 1; S <= y.smax; ++S) {
+      const int kps = static_cast<int>(ceil_div(y.k_tiles, S));
+      if (ceil_div(y.k_tiles, kps) != S) continue;  // a split would be empty
+      const int64_t items = static_cast<int64_t>(y.tiles) * S;
+      if (S > 1 && items > cap) continue;
+      const int64_t waves = ceil_div(items, cap);
+      const int64_t cost = waves * kps * 250 + (S > 1 ? 700 : 0);
+      if (best_cost < 0 || cost < best_cost) {
+        best_cost = cost;
+        best = S;
+      }
+    }
+    pl->splits[l] = best;
+    const int64_t items = static_cast<int64_t>(y.tiles) * best;
+    grid = static_cast<int>(std::max<int64_t>(grid, std::min<int64_t>(items, cap)));
+  }
+  pl->stages = stages;
+  pl->smem = smem;
+  pl->tmem_cols = tcols;
+  pl->grid = grid;
+  return true;
+}
+
 }  // namespace
 
 void set_last_error(const char* what) { snprintf(g_last_error, sizeof(g_last_error), "%s", what); }
@@ -513,6 +668,116 @@ mxfp4_status_t mxfp4_gemm_with_plan(const void* A_or_Aq, int64_t lda, const void
   if (plan == nullptr) return MXFP4_ERR_INVALID_ARG;
   return run_gemm(A_or_Aq, fused ? lda : K / 2, As, Bpacked, C, M, N, K, fused != 0, plan,
                   reinterpret_cast<cudaStream_t>(stream));
+}
+
+size_t mxfp4_chain_workspace_bytes(int64_t M, int64_t K, int32_t num_layers, const int64_t* N) {
+  if (num_layers < 1 || num_layers > kMaxChainLayers || N == nullptr) return 0;
+  for (int l = 0; l < num_layers; ++l) {
+    const int64_t K_l = l == 0 ? K : N[l - 1];
+    if (check_mnk(M, N[l], K_l) != MXFP4_OK) return 0;
+  }
+  ChainGeometry g;
+  chain_geometry(M, K, num_layers, N, &g);
+  return g.total;
+}
+
+mxfp4_status_t mxfp4_quant_gemm_chain(const void* A, int64_t lda, int64_t M, int64_t K, int32_t num_layers,
+                                      const void* const* Bpacked, const int64_t* N, void* const* C, void* ws,
+                                      size_t ws_bytes, mxfp4_stream_t stream) {
+  mxfp4_status_t st = check_chain_args(A, lda, M, K, num_layers, Bpacked, N, C);
+  if (st != MXFP4_OK) return st;
+  ChainGeometry g;
+  chain_geometry(M, K, num_layers, N, &g);
+  if (ws == nullptr) return MXFP4_ERR_INVALID_ARG;
+  if (ws_bytes < g.total) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MXFP4_ERR_MISALIGNED;
+  const DeviceInfo* dev = current_device(&st);
+  if (dev == nullptr) return st;
+  ChainPlan pl;
+  if (!chain_plan(g, dev->prop, &pl)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  uint32_t* counters = reinterpret_cast<uint32_t*>(base + g.counters);
+  ChainArgs a;
+  memset(&a, 0, sizeof(a));
+  for (int l = 0; l < num_layers; ++l) {
+    const ChainGeometry::Layer& y = g.layer[l];
+    ChainLayerArgs& L = a.layer[l];
+    if (!encode_weight_map(Bpacked[l], y.N, y.K, &a.wmap[l])) return failure("cuTensorMapEncodeTiled (weights)");
+    if (!encode_activation_map(base + y.codes, M, y.K, y.K / 2, false, g.bm, &a.amap[l]))
+      return failure("cuTensorMapEncodeTiled (activation codes)");
+    L.b_sf = static_cast<const uint8_t*>(Bpacked[l]) + packed_layout(y.N, y.K).sf_offset;
+    L.c = static_cast<__nv_bfloat16*>(C[l]);
+    L.in_sf = base + y.sf;
+    L.in_done = counters + y.done;
+    L.in_n_tiles = l == 0 ? 0 : g.layer[l - 1].n_tiles;
+    if (l + 1 < num_layers) {
+      const ChainGeometry::Layer& nx = g.layer[l + 1];
+      L.out_codes = base + nx.codes;
+      L.out_sf = base + nx.sf;
+      L.out_done = counters + nx.done;
+      L.k_tiles_next = nx.k_tiles;
+    }
+    L.partials = reinterpret_cast<float*>(base + y.part);
+    L.tickets = counters + y.tickets;
+    L.N = static_cast<int32_t>(y.N);
+    L.K = static_cast<int32_t>(y.K);
+    L.k_tiles = y.k_tiles;
+    L.splits = pl.splits[l];
+    L.kt_per_split = static_cast<int32_t>(ceil_div(y.k_tiles, pl.splits[l]));
+    L.n_tiles = y.n_tiles;
+    L.items = y.tiles * pl.splits[l];
+  }
+  a.a = static_cast<const uint16_t*>(A);
+  a.lda = lda;
+  a.a_codes = base + g.layer[0].codes;
+  a.a_sf = base + g.layer[0].sf;
+  a.a_done = counters + g.layer[0].done;
+  a.counters = counters;
+  a.n_counters = static_cast<int32_t>(g.n_counters);
+  a.exit_count = counters + (g.n_counters - 1);
+  a.err = device_error_word();
+  if (a.err == nullptr) return failure("cudaGetSymbolAddress (device error word)");
+  a.timeout_ns = g_timeout_ns.load();
+  a.layers = num_layers;
+  a.M = static_cast<int32_t>(M);
+  a.K0 = static_cast<int32_t>(K);
+  a.k_tiles0 = g.layer[0].k_tiles;
+  a.m_tiles = g.m_tiles;
+  a.stages = pl.stages;
+  a.a_box_rows = activation_box_rows(M, g.bm);
+  a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
+  uint32_t offs[4];
+  int smem = 0, tcols = 0;
+  chain_smem(g.bm, pl.stages, dev->prop, &smem, &tcols, offs);
+  a.a_off = offs[0];
+  a.sfw_off = offs[1];
+  a.sfa_off = offs[2];
+  a.bar_off = offs[3];
+  a.weights_early = g_programmatic.load() >= 2 ? 1 : 0;
+  const cudaError_t e = launch_chain(a, g.bm, pl.grid, pl.smem, g_programmatic.load() != 0,
+                                     reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? MXFP4_OK : cuda_failure("multi-layer launch", e);
+}
+
+mxfp4_status_t mxfp4_chain_plan(int64_t M, int64_t K, int32_t num_layers, const int64_t* N, int32_t* splits,
+                                int32_t* grid, int32_t* block_m) {
+  if (num_layers < 1 || num_layers > kMaxChainLayers || N == nullptr) return MXFP4_ERR_INVALID_ARG;
+  for (int l = 0; l < num_layers; ++l) {
+    const int64_t K_l = l == 0 ? K : N[l - 1];
+    mxfp4_status_t st = check_mnk(M, N[l], K_l);
+    if (st != MXFP4_OK) return st;
+  }
+  mxfp4_status_t st;
+  const DeviceInfo* dev = current_device(&st);
+  if (dev == nullptr) return st;
+  ChainGeometry g;
+  chain_geometry(M, K, num_layers, N, &g);
+  ChainPlan pl;
+  if (!chain_plan(g, dev->prop, &pl)) return MXFP4_ERR_UNSUPPORTED_SHAPE;
+  for (int l = 0; l < num_layers && splits != nullptr; ++l) splits[l] = pl.splits[l];
+  if (grid != nullptr) *grid = pl.grid;
+  if (block_m != nullptr) *block_m = g.bm;
+  return MXFP4_OK;
 }
 
 const char* mxfp4_status_string(mxfp4_status_t status) {

@@ -118,6 +118,51 @@ cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, co
                         const GemmArgs& args, const mxfp4_plan_t& plan, bool fused, bool programmatic,
                         cudaStream_t s);
 
+// ----------------------------------------------------------------------------- multi-layer kernel
+// Layers one launch of the multi-layer kernel can run.
+constexpr int kMaxChainLayers = 16;
+
+// One layer of a multi-layer launch (device addresses; see chain.cu).
+struct ChainLayerArgs {
+  const uint8_t* b_sf;       // packed weight scales
+  __nv_bfloat16* c;          // output C [M, N]
+  const uint8_t* in_sf;      // this layer's activation scale chunks [m_tiles][k_tiles][1 KB]
+  const uint32_t* in_done;   // [m_tiles][k_tiles]: readiness of the activation, per K tile
+  uint8_t* out_codes;        // next layer's activation codes [M, N/2] (null on the last layer)
+  uint8_t* out_sf;           // next layer's activation scale chunks [m_tiles][k_tiles_next][1 KB]
+  uint32_t* out_done;        // [m_tiles][k_tiles_next]
+  float* partials;           // split-K partials [tiles][splits][block_m][128] fp32
+  uint32_t* tickets;         // [tiles]: splits that have stored their partial
+  int32_t N, K, k_tiles, kt_per_split, splits, n_tiles, items;
+  int32_t in_n_tiles;        // N tiles of the layer producing this one's input (0: the first layer)
+  int32_t k_tiles_next;
+};
+
+struct ChainArgs {
+  CUtensorMap wmap[kMaxChainLayers];  // weight codes, per layer
+  CUtensorMap amap[kMaxChainLayers];  // activation codes in the workspace, per layer
+  ChainLayerArgs layer[kMaxChainLayers];
+  const uint16_t* a;         // bf16 A [M, lda] (the first layer's input)
+  int64_t lda;
+  uint8_t* a_codes;          // the first layer's activation codes [M, K/2]
+  uint8_t* a_sf;             // ... and scale chunks
+  uint32_t* a_done;          // ... and their readiness counters
+  uint32_t* counters;        // every counter of the workspace (zeroed by the last CTA to finish)
+  uint32_t* exit_count;
+  uint32_t* err;
+  uint64_t timeout_ns;
+  int32_t n_counters;
+  int32_t layers, M, K0, k_tiles0, m_tiles, stages, a_box_rows;
+  uint32_t tmem_cols;
+  uint32_t a_off, sfw_off, sfa_off, bar_off;
+  int32_t weights_early;
+};
+
+cudaError_t launch_chain(const ChainArgs& args, int block_m, int grid, int smem_bytes, bool programmatic,
+                         cudaStream_t s);
+// Blocks of the multi-layer kernel that fit on one SM with this shared memory.
+int chain_blocks_per_sm(int block_m, int smem_bytes);
+
 cudaError_t read_device_error(cudaStream_t s, uint32_t* code, bool reset);
 // The size checks every GEMM entry makes: MXFP4_ERR_INVALID_ARG for
 // non-positive sizes or K % 32 != 0, MXFP4_ERR_UNSUPPORTED_SHAPE past the

@@ -19,6 +19,7 @@ enum DeviceError : uint32_t {
   kErrWaitDrain = 1u << 4,   // teardown waiting for copies in flight
   kErrDiag = 1u << 5,        // the diagnostic kernel's wait (expected to give up)
   kErrBadPlan = 1u << 6,     // launch geometry disagrees with the kernel
+  kErrWaitFlag = 1u << 7,    // a wait on another CTA's completion counter (multi-layer kernel)
 };
 
 __device__ __forceinline__ void report_error(uint32_t* word, uint32_t bits) {
@@ -220,6 +221,56 @@ __device__ __forceinline__ uint2 ld_after_wait_v2(const void* p) {
 __device__ __forceinline__ uint32_t ld_after_wait_u8(const void* p) {
   uint32_t v;
   asm volatile("ld.global.cg.u8 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// ----------------------------------------------------------------------------- counters between CTAs
+// Completion counters in global memory that one CTA releases and others wait
+// for (the multi-layer kernel's layer-to-layer hand-off).  The producer's
+// threads store their results, then each makes them visible at GPU scope
+// (fence_proxy_async_global for later TMA readers, then __threadfence), the
+// CTA synchronises, and one thread adds to the counter with release
+// semantics.  A consumer thread polls with acquire loads, then orders its own
+// later TMA reads after the acquire with fence_proxy_async_global.
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(uint32_t* p, uint32_t v) {
+  uint32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Orders this thread's generic-proxy global accesses with its async-proxy
+// (TMA, bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Waits until the counter equals `target` exactly, for at most timeout_ns of
+// global time; false if it gave up.  Equality, not >=: each counter receives
+// exactly its expected number of increments per launch, so a value past the
+// target means the counters did not start at zero (an uncleared workspace),
+// which then ends in a reported timeout instead of a wrong result.
+__device__ __forceinline__ bool wait_count_eq(const uint32_t* p, uint32_t target, uint64_t timeout_ns) {
+  if (ld_acquire_gpu(p) == target) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t it = 1;; ++it) {
+    if (ld_acquire_gpu(p) == target) return true;
+    if ((it & 15u) == 0 && global_timer_ns() - t0 > timeout_ns) return false;
+  }
+}
+
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
 

@@ -78,4 +78,22 @@ __device__ __forceinline__ uint32_t e2m1_pack8(uint4 v, uint16_t scale_bf16) {
   return out;
 }
 
+// Two bf16 values (pair: element 2i in the low half, 2i + 1 in the high half)
+// times 2^-s -> one byte of two E2M1 codes, element 2i in the low nibble: the
+// same instructions as e2m1_pack8, for one pair.
+__device__ __forceinline__ uint32_t e2m1_pack2(uint32_t pair, uint16_t scale_bf16) {
+  uint32_t out;
+  asm("{\n\t.reg .b16 l0, h0;\n\t"
+      ".reg .f32 y0, y1;\n\t"
+      ".reg .b8 c0;\n\t"
+      "mov.b32 {l0, h0}, %1;\n\t"
+      "fma.rn.f32.bf16 y0, l0, %2, 0f80000000;\n\t"
+      "fma.rn.f32.bf16 y1, h0, %2, 0f80000000;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 c0, y1, y0;\n\t"
+      "cvt.u32.u8 %0, c0;\n\t}"
+      : "=r"(out)
+      : "r"(pair), "h"(scale_bf16));
+  return out;
+}
+
 }  // namespace mxfp4

@@ -221,6 +221,59 @@ mxfp4_status_t mxfp4_quant_gemm_host(const void* A_host, int64_t lda_host, void*
 mxfp4_status_t mxfp4_quant_gemm_static_scratch(const void* A, int64_t lda, const void* Bpacked, void* C,
                                                int64_t M, int64_t N, int64_t K, mxfp4_stream_t stream);
 
+/* ---------------------------------------------------------------------------
+ * mxfp4_quant_gemm_chain -- several dependent layers in one launch.
+ *
+ * Layer l computes C_l = quant(X_l) * B_l^T (the fused layer above), with
+ * X_0 = A and X_l = C_{l-1} for l >= 1: K_0 = K, K_l = N_{l-1}.  The pages run
+ * one quantize + GEMM per layer and find most of each call's time in the
+ * per-launch cost (submission 733989, "PROFILING"; submission 755056 captures
+ * its launches in a CUDA graph for the same reason); here one persistent
+ * kernel runs every layer: its CTAs stay resident, each layer waits only for
+ * the K tiles of its input that it reads (bounded device-side waits on
+ * completion counters), the next layer's weights load while the current
+ * layer finishes, and each layer's epilogue quantizes its own bf16 output
+ * for the next layer (bit-identical to mxfp4_quantize of C_l).  The first
+ * layer's activation is quantized once, shared by all CTAs.
+ *
+ *   A        device, bf16 [M, lda]; lda >= K, lda % 8 == 0
+ *   M, K     rows of every X_l / C_l, and the first layer's K (K % 32 == 0)
+ *   num_layers  1 .. 16
+ *   Bpacked  host array of num_layers device pointers: the packed weights
+ *            [N_l, K_l] (mxfp4_pack_weights)
+ *   N        host array of num_layers output widths; N_l % 32 == 0 for every
+ *            layer but the last (N_l is the next layer's K)
+ *   C        host array of num_layers device pointers, bf16 [M, N_l]
+ *            row-major, every layer's output written
+ *   ws, ws_bytes  device workspace of at least
+ *            mxfp4_chain_workspace_bytes(M, K, num_layers, N) bytes, 256-byte
+ *            aligned, and ZERO-INITIALISED before its first use (cudaMemset).
+ *            It holds each layer's activation codes, split-K partials and
+ *            the completion counters; every call returns the counters to
+ *            zero, so one zeroing serves any number of calls with the same
+ *            workspace.  Calls sharing a workspace must be ordered (one
+ *            stream).  If a call's device-side wait runs out (see
+ *            mxfp4_device_error), zero the workspace again.  A workspace that
+ *            was not zeroed makes the kernel's waits run out and report,
+ *            instead of producing a wrong result.
+ * Rows of C_l are identical in meaning to mxfp4_quant_gemm's on the same
+ * input; values agree within fp32 summation order (K splits may differ).
+ * Every CTA must be resident at once (the grid is at most one wave of the
+ * device); kernels of other streams that hold SMs for longer than the wait
+ * limit make the call report a timeout.  Errors as for the other entries:
+ * nothing launched unless MXFP4_OK. */
+size_t mxfp4_chain_workspace_bytes(int64_t M, int64_t K, int32_t num_layers, const int64_t* N);
+
+mxfp4_status_t mxfp4_quant_gemm_chain(const void* A, int64_t lda, int64_t M, int64_t K, int32_t num_layers,
+                                      const void* const* Bpacked, const int64_t* N, void* const* C, void* ws,
+                                      size_t ws_bytes, mxfp4_stream_t stream);
+
+/* The plan of a multi-layer launch: per layer its K split count (splits, a
+ * host array of num_layers, may be NULL), the grid size and the rows of
+ * activation per CTA.  Host only, launches nothing. */
+mxfp4_status_t mxfp4_chain_plan(int64_t M, int64_t K, int32_t num_layers, const int64_t* N, int32_t* splits,
+                                int32_t* grid, int32_t* block_m);
+
 /* The plan the two GEMM entries would use for (M, N, K); fused != 0 for the
  * fused entry.  Host only, launches nothing. */
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan);

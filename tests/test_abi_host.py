@@ -149,3 +149,64 @@ def test_prepared_calls_check_their_arguments_once():
     with pytest.raises(TypeError):  # A_dev on the host
         mx.prepare_quant_gemm_host(cpu, W, cpu, cpu, torch.zeros(4, 128, dtype=torch.bfloat16))
 
+
+
+def chain_workspace_expected(M: int, K: int, Ns: list[int]) -> int:
+    """The multi-layer workspace, restated: per layer codes, scale chunks and
+    split-K partials (for up to min(8, K tiles) splits), then the counters."""
+    a256 = lambda x: -(-x // 256) * 256
+    bm = 16 if M <= 16 else 32 if M <= 32 else 64
+    mt = -(-M // bm)
+    total, counters, k = 0, 0, K
+    for n in Ns:
+        kt, nt = -(-k // 256), -(-n // 128)
+        smax = min(8, kt)
+        total += a256(M * k // 2) + a256(mt * kt * 1024)
+        if smax > 1:
+            total += a256(nt * mt * smax * bm * 128 * 4)
+        counters += mt * kt + nt * mt
+        k = n
+    return total + a256((counters + 1) * 4)
+
+
+def test_chain_workspace_bytes(lib):
+    fn = lib.mxfp4_chain_workspace_bytes
+    fn.restype = ctypes.c_size_t
+    for M, K, Ns in ((32, 512, [4096, 512]), (5, 96, [160, 64, 33]), (256, 1536, [3072, 1536]), (1, 32, [32]),
+                     (100, 288, [256, 96, 200])):
+        arr = (ctypes.c_int64 * len(Ns))(*Ns)
+        assert fn(M, K, len(Ns), arr) == chain_workspace_expected(M, K, Ns), (M, K, Ns)
+    arr = (ctypes.c_int64 * 2)(100, 64)
+    assert fn(4, 512, 2, arr) == 0  # layer 1's K = 100 is not a multiple of 32
+    assert fn(4, 512, 0, arr) == 0
+    assert fn(4, 512, 17, (ctypes.c_int64 * 17)(*([512] * 17))) == 0
+
+
+def test_chain_argument_checks_launch_nothing(lib):
+    fake = 0x10000
+    fn = lib.mxfp4_quant_gemm_chain
+    P = ctypes.c_void_p
+
+    def call(A=fake, lda=512, M=32, K=512, Ns=(4096, 512), B=None, C=None, ws=fake, ws_bytes=1 << 30,
+             L=None):
+        L = len(Ns) if L is None else L
+        n = (ctypes.c_int64 * max(1, len(Ns)))(*Ns)
+        b = (P * max(1, len(Ns)))(*([fake] * len(Ns) if B is None else B))
+        c = (P * max(1, len(Ns)))(*([fake] * len(Ns) if C is None else C))
+        return fn(A, lda, M, K, L, b, n, c, ws, ws_bytes, None)
+
+    assert call(L=0) == INVALID
+    assert call(L=17, Ns=[512] * 17) == INVALID
+    assert call(A=None) == INVALID
+    assert call(lda=256) == INVALID  # lda < K
+    assert call(K=48) == INVALID
+    assert call(Ns=(100, 512)) == INVALID  # layer 1's K = N_0 not a multiple of 32
+    assert call(B=[fake, None]) == INVALID
+    assert call(C=[None, fake]) == INVALID
+    assert call(ws=None) == INVALID
+    assert call(ws_bytes=1024) == WS_SMALL
+    assert call(ws=fake + 16) == MISALIGNED  # the workspace must be 256-byte aligned
+    assert call(A=fake + 8) == MISALIGNED
+    assert call(lda=516) == MISALIGNED
+    assert call(C=[fake, fake + 8]) == MISALIGNED
+    assert call(M=1 << 20, Ns=(1 << 12, 512)) == UNSUPPORTED  # M * N > 2^31
