@@ -416,7 +416,8 @@ void chain_smem(int bm, int stages, const cudaDeviceProp& prop, int* smem, int* 
   const uint32_t a_off = st * kTileN * kTileKBytes;
   const uint32_t sfw_off = a_off + st * static_cast<uint32_t>(bm) * kTileKBytes;
   const uint32_t sfa_off = sfw_off + st * kSfTileBytes;
-  const uint32_t bar_off = sfa_off + st * 2 * kSfChunkBytes;
+  const uint32_t epi_off = sfa_off + st * 2 * kSfChunkBytes;  // the epilogue's bf16 tile [bm][128]
+  const uint32_t bar_off = epi_off + static_cast<uint32_t>(bm) * kTileN * 2;
   const uint32_t total = bar_off + (3 * st + 2) * 8 + 16;
   uint32_t t = 32;
   while (t < static_cast<uint32_t>(bm + 16 * stages)) t <<= 1;
@@ -432,7 +433,8 @@ void chain_smem(int bm, int stages, const cudaDeviceProp& prop, int* smem, int* 
     offs[0] = a_off;
     offs[1] = sfw_off;
     offs[2] = sfa_off;
-    offs[3] = bar_off;
+    offs[3] = epi_off;
+    offs[4] = bar_off;
   }
 }
 
@@ -440,7 +442,8 @@ void chain_smem(int bm, int stages, const cudaDeviceProp& prop, int* smem, int* 
 // then per layer the K split minimising an estimate of one item's critical
 // path (~250 ns per K tile in sequence, ~700 ns for the split-K sum) among
 // splits whose items all fit in one wave; the grid is the largest layer's
-// item count (at most one wave).
+// item count (at most one wave).  When that grid needs at most one CTA per
+// SM, the ring deepens to what one CTA per SM can hold (up to 8 stages).
 bool chain_plan(const ChainGeometry& g, const cudaDeviceProp& prop, ChainPlan* pl) {
   int stages = 6, smem = 0, tcols = 0;
   for (; stages >= 2; --stages) {
@@ -486,6 +489,20 @@ bool chain_plan(const ChainGeometry& g, const cudaDeviceProp& prop, ChainPlan* p
     pl->splits[l] = best;
     const int64_t items = static_cast<int64_t>(y.tiles) * best;
     grid = static_cast<int>(std::max<int64_t>(grid, std::min<int64_t>(items, cap)));
+  }
+  // A grid of one CTA per SM at most leaves each CTA a whole SM: a deeper ring
+  // (up to 8 K tiles: an item and the next layer's weights in flight).
+  if (grid <= prop.multiProcessorCount) {
+    for (int st = 8; st > stages; --st) {
+      int sm1 = 0, tc1 = 0;
+      chain_smem(g.bm, st, prop, &sm1, &tc1, nullptr);
+      if (sm1 <= static_cast<int>(prop.sharedMemPerBlockOptin) && tc1 <= 512 && chain_blocks_per_sm(g.bm, sm1) >= 1) {
+        stages = st;
+        smem = sm1;
+        tcols = tc1;
+        break;
+      }
+    }
   }
   pl->stages = stages;
   pl->smem = smem;
@@ -710,6 +727,7 @@ mxfp4_status_t mxfp4_quant_gemm_chain(const void* A, int64_t lda, int64_t M, int
     L.in_sf = base + y.sf;
     L.in_done = counters + y.done;
     L.in_n_tiles = l == 0 ? 0 : g.layer[l - 1].n_tiles;
+    L.in_splits = l == 0 ? 1 : pl.splits[l - 1];
     if (l + 1 < num_layers) {
       const ChainGeometry::Layer& nx = g.layer[l + 1];
       L.out_codes = base + nx.codes;
@@ -746,13 +764,14 @@ mxfp4_status_t mxfp4_quant_gemm_chain(const void* A, int64_t lda, int64_t M, int
   a.stages = pl.stages;
   a.a_box_rows = activation_box_rows(M, g.bm);
   a.tmem_cols = static_cast<uint32_t>(pl.tmem_cols);
-  uint32_t offs[4];
+  uint32_t offs[5];
   int smem = 0, tcols = 0;
   chain_smem(g.bm, pl.stages, dev->prop, &smem, &tcols, offs);
   a.a_off = offs[0];
   a.sfw_off = offs[1];
   a.sfa_off = offs[2];
-  a.bar_off = offs[3];
+  a.epi_off = offs[3];
+  a.bar_off = offs[4];
   a.weights_early = g_programmatic.load() >= 2 ? 1 : 0;
   const cudaError_t e = launch_chain(a, g.bm, pl.grid, pl.smem, g_programmatic.load() != 0,
                                      reinterpret_cast<cudaStream_t>(stream));

@@ -26,14 +26,17 @@
 //     layout) and scales (bulk copy); warp 1 issues the block-scaled MMAs
 //     into a tensor-memory accumulator; warps 2-9 run the epilogue;
 //   - K splits (for layers with few output tiles and long K) store fp32
-//     partials in the workspace; the last split of a tile to arrive sums all
-//     of them in split order (deterministic) and runs the epilogue;
+//     partials in the workspace; once every split of a tile has, each split
+//     CTA sums a share of the tile over all partials in split order
+//     (deterministic) and runs the epilogue on it;
 //   - every counter returns to zero at the end of the launch (the last CTA to
 //     finish clears them), so the workspace needs zeroing only once.
 //
 // Every wait is bounded; a wait that gives up sets the device error word and
 // the CTA skips the rest of its work, still draining its copies, freeing its
 // tensor memory and taking part in the final counter reset.
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 #include "quant.cuh"
@@ -117,7 +120,7 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
     int t = 0;
     bool stop = false;
     for (int l = 0; l < layers && !stop; ++l) {
-      const ChainLayerArgs& L = p.layer[l];
+      const ChainLayerArgs L = p.layer[l];  // a copy: read once, not through a param-space pointer
       for (int i = b; i < L.items && !stop; i += G) {
         const ChainItem it = chain_item(L, i);
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++t) {
@@ -157,7 +160,7 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
     int t = 0;
     bool stop = false;
     for (int l = 0; l < layers && !stop; ++l) {
-      const ChainLayerArgs& L = p.layer[l];
+      const ChainLayerArgs L = p.layer[l];  // a copy: read once, not through a param-space pointer
       for (int i = b; i < L.items && !stop; i += G) {
         const ChainItem it = chain_item(L, i);
         for (int kt = it.kt0; kt < it.kt1; ++kt, ++t) {
@@ -167,8 +170,9 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
           uint32_t err_bit = kErrWaitEmpty;
           if (lane == 0 && ok) {
             // the activation's K tile: every producer of it has released its counter
+            // (each split CTA of a producer tile counts its share of the tile)
             const uint32_t expect = L.in_n_tiles == 0 ? static_cast<uint32_t>(BM / 16)
-                                                      : static_cast<uint32_t>(min(2, L.in_n_tiles - 2 * kt));
+                                                      : static_cast<uint32_t>(min(2, L.in_n_tiles - 2 * kt) * L.in_splits);
             ok = wait_count_eq(L.in_done + static_cast<size_t>(it.m_tile) * L.k_tiles + kt, expect, timeout);
             err_bit = kErrWaitFlag;
             if (ok) {
@@ -201,7 +205,7 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
     const bool leader = elect_one();
     int t = 0, item_idx = 0;
     for (int l = 0; l < layers; ++l) {
-      const ChainLayerArgs& L = p.layer[l];
+      const ChainLayerArgs L = p.layer[l];  // a copy: read once, not through a param-space pointer
       const int K = L.K;
       for (int i = b; i < L.items; i += G, ++item_idx) {
         const ChainItem it = chain_item(L, i);
@@ -302,18 +306,18 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
           p.a_sf[(static_cast<size_t>(m_tile) * p.k_tiles0 + kt) * kChainATileSf + (blk >> 2) * kSfChunkBytes +
                  sf_chunk_offset(r_t) + (blk & 3)] = static_cast<uint8_t>(byte);
         }
-        fence_proxy_async_global();
-        __threadfence();
-        named_barrier(1, kChainEpiThreads);
+        fence_proxy_async_global();  // read by TMA in other CTAs
+        named_barrier(1, kChainEpiThreads);  // every thread's stores, then one release add
         if (tid == 0) red_release_gpu_add(p.a_done + static_cast<size_t>(m_tile) * p.k_tiles0 + kt, 1u);
       }
     }
 
     const int q = warp & 3;  // tensor-memory lane quarter this warp may read: output columns 32q..32q+31
     const int h = ew >> 2;   // which half of the 16-row chunks
+    uint16_t* ctile = reinterpret_cast<uint16_t*>(smem + p.epi_off);  // bf16 [BM][128]: this CTA's finished rows
     int item_idx = 0;
     for (int l = 0; l < layers; ++l) {
-      const ChainLayerArgs& L = p.layer[l];
+      const ChainLayerArgs L = p.layer[l];  // a copy: read once, not through a param-space pointer
       const int N = L.N;
       const bool quant_next = L.out_codes != nullptr;
       for (int i = b; i < L.items; i += G, ++item_idx) {
@@ -321,8 +325,7 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
         const int m_base = it.m_tile * BM;
         const int m_valid = min(BM, M - m_base);
         const int chunks = (m_valid + 15) >> 4;
-        const int n_warp = it.n_tile * kTileN + 32 * q;  // this warp's first output column
-        const int n = n_warp + lane;
+        const int n_base = it.n_tile * kTileN;
         const bool ok = mbar_wait(accum_full, item_idx & 1, timeout);
         if (!ok) {
           report_error(p.err, kErrWaitAccum);
@@ -334,39 +337,57 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
         named_barrier(1, kChainEpiThreads);
         const bool alive = *shared_flag != 0u;
 
-        // bf16 results of one 16-row chunk (r[e]: row 16c + e, this lane's
-        // column) to C and, unless this is the last layer, to the next
-        // layer's codes and scale chunk
-        auto finish = [&](const float (&r)[16], int c) {
-          uint16_t* crow = reinterpret_cast<uint16_t*>(L.c) + static_cast<int64_t>(m_base) * N + n;
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int m = 16 * c + e;
-            if (m >= m_valid) break;  // warp-uniform
-            const uint32_t bf = __bfloat16_as_ushort(__float2bfloat16_rn(r[e]));
-            if (n < N) crow[static_cast<int64_t>(m) * N] = static_cast<uint16_t>(bf);
-            if (quant_next) {
-              // one 32-element block of the next layer's K: the warp's 32 columns
-              const uint32_t amax = __reduce_max_sync(0xFFFFFFFFu, bf & 0x7FFFu);
-              const uint32_t byte = scale_byte_from_amax(amax);
-              const uint16_t sbf = scale_bf16_from_byte(byte);
-              const uint32_t odd = __shfl_down_sync(0xFFFFFFFFu, bf, 1);
-              const uint32_t code = e2m1_pack2(bf | (odd << 16), sbf);  // lanes 2i: columns 2i, 2i + 1
-              const uint32_t word = code | (__shfl_down_sync(0xFFFFFFFFu, code, 2) << 8) |
-                                    (__shfl_down_sync(0xFFFFFFFFu, code, 4) << 16) |
-                                    (__shfl_down_sync(0xFFFFFFFFu, code, 6) << 24);
-              if ((lane & 7) == 0 && n_warp < N)  // N % 32 == 0: the warp's columns are all in or all out
-                *reinterpret_cast<uint32_t*>(L.out_codes + static_cast<int64_t>(m_base + m) * (N / 2) + n / 2) = word;
-              if (lane == 0)
-                L.out_sf[(static_cast<size_t>(it.m_tile) * L.k_tiles_next + (it.n_tile >> 1)) * kChainATileSf +
-                         (it.n_tile & 1) * kSfChunkBytes + sf_chunk_offset(m) + q] = static_cast<uint8_t>(byte);
+        // One finished value (row m of the tile, column nl), rounded to bf16,
+        // into the staged tile.
+        auto put = [&](float v, int m, int nl) { ctile[m * kTileN + nl] = __bfloat16_as_ushort(__float2bfloat16_rn(v)); };
+        // The staged rows the predicate selects, out: to C (16 bytes at a time
+        // where N allows), and, unless this is the last layer, as the next
+        // layer's codes and scales -- one thread per 16 elements, two per
+        // 32-element block (the quantize kernel's scheme and arithmetic, on the
+        // bf16 values of C).  When quantizing, N % 32 == 0, so a block is wholly
+        // inside or past N; blocks past N hold zeros (padding weight rows) and
+        // get scale byte 0.
+        auto write_rows = [&](int units, auto row_of) {
+          const int span = (units + 31) / 32 * 32;  // whole warps: the pair shuffle needs every lane
+          const bool vec = N % 8 == 0;
+          for (int u = tid; u < span; u += kChainEpiThreads) {
+            const int m = u < units ? row_of(u >> 3) : 0, j = u & 7;
+            const bool valid = u < units && m < m_valid;
+            const int n0 = n_base + 16 * j;
+            uint4 v = make_uint4(0, 0, 0, 0), w = make_uint4(0, 0, 0, 0);
+            if (valid) {
+              const uint4* src = reinterpret_cast<const uint4*>(ctile + m * kTileN + 16 * j);
+              v = src[0];
+              w = src[1];
+              uint16_t* crow = reinterpret_cast<uint16_t*>(L.c) + static_cast<int64_t>(m_base + m) * N;
+              if (vec && n0 + 16 <= N) {
+                *reinterpret_cast<uint4*>(crow + n0) = v;
+                *reinterpret_cast<uint4*>(crow + n0 + 8) = w;
+              } else if (vec && n0 + 8 <= N) {
+                *reinterpret_cast<uint4*>(crow + n0) = v;
+              } else if (n0 < N) {
+                const uint16_t* e16 = ctile + m * kTileN + 16 * j;
+                for (int e = 0; e < 16 && n0 + e < N; ++e) crow[n0 + e] = e16[e];
+              }
             }
+            if (!quant_next) continue;  // uniform
+            uint32_t amax = absmax16_bf16(v, w);
+            amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            const uint32_t byte = scale_byte_from_amax(amax);
+            const uint16_t sbf = scale_bf16_from_byte(byte);
+            const uint32_t c0 = e2m1_pack8(v, sbf), c1 = e2m1_pack8(w, sbf);
+            if (valid && n_base + 16 * j < N)
+              *reinterpret_cast<uint2*>(L.out_codes + static_cast<int64_t>(m_base + m) * (N / 2) + n_base / 2 + 8 * j) =
+                  make_uint2(c0, c1);
+            if (valid && (j & 1) == 0)
+              L.out_sf[(static_cast<size_t>(it.m_tile) * L.k_tiles_next + (it.n_tile >> 1)) * kChainATileSf +
+                       (it.n_tile & 1) * kSfChunkBytes + sf_chunk_offset(m) + (j >> 1)] = static_cast<uint8_t>(byte);
           }
         };
-        // makes this tile's results visible, then counts the tile done
+        // Counts this CTA's part of the tile done.  The CTA barrier orders every
+        // thread's stores before the single release add (release is cumulative).
         auto release = [&]() {
-          fence_proxy_async_global();
-          __threadfence();
+          fence_proxy_async_global();  // codes and scales are read by TMA in other CTAs
           named_barrier(1, kChainEpiThreads);
           if (tid == 0 && alive && L.out_done != nullptr)
             red_release_gpu_add(L.out_done + static_cast<size_t>(it.m_tile) * L.k_tiles_next + (it.n_tile >> 1), 1u);
@@ -375,23 +396,28 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
         if (L.splits == 1) {
 #pragma unroll 1
           for (int c = h; c < chunks; c += 2) {
+            if (!alive) break;
             uint32_t r[16];
-            float f[16];
-            if (alive) {
-              tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
-              tmem_ld_wait();
+            tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
+            tmem_ld_wait();
 #pragma unroll
-              for (int e = 0; e < 16; ++e) f[e] = __uint_as_float(r[e]);
-              finish(f, c);
-            }
+            for (int e = 0; e < 16; ++e)
+              if (16 * c + e < m_valid) put(__uint_as_float(r[e]), 16 * c + e, 32 * q + lane);
           }
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(tmem_empty);
+          named_barrier(1, kChainEpiThreads);  // the staged tile is complete
+          if (alive) write_rows(m_valid * 8, [](int row) { return row; });
           release();
         } else {
+          // K split: every split stores its fp32 partial; once all S have
+          // (a count per tile), split CTA s finishes the tile's 4-row groups
+          // g = s, s + S, ..., each value the sum of the S partials in split
+          // order (deterministic: the same order whichever CTA sums).
+          const int S = L.splits;
           const int tile = it.m_tile * L.n_tiles + it.n_tile;
-          float* part = L.partials + static_cast<size_t>(tile) * L.splits * BM * kTileN;
+          float* part = L.partials + static_cast<size_t>(tile) * S * BM * kTileN;
 #pragma unroll 1
           for (int c = h; c < chunks; c += 2) {
             if (!alive) break;
@@ -406,31 +432,66 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
           tc_fence_before_sync();
           __syncwarp();
           if (lane == 0) mbar_arrive(tmem_empty);
-          __threadfence();
           named_barrier(1, kChainEpiThreads);
           if (tid == 0) {
-            // the last split to arrive sums every partial, in split order
-            const bool last = alive && atom_add_acq_rel_gpu(L.tickets + tile, 1u) == static_cast<uint32_t>(L.splits - 1);
-            *shared_flag = last ? 1u : 0u;
+            bool all = false;
+            if (alive) {
+              red_release_gpu_add(L.tickets + tile, 1u);
+              all = wait_count_eq(L.tickets + tile, static_cast<uint32_t>(S), timeout);
+              if (!all) {
+                report_error(p.err, kErrWaitFlag);
+                *abort_flag = 1u;
+              }
+            }
+            *shared_flag = all ? 1u : 0u;
           }
           named_barrier(1, kChainEpiThreads);
-          if (*shared_flag != 0u) {
+          const bool summing = *shared_flag != 0u;
+          const int groups = (m_valid + 3) >> 2;
+          const int mine = summing && it.split < groups ? (groups - it.split + S - 1) / S : 0;
+          // 16 pieces (row, 32 columns) per group, piece p of the CTA's groups
+          // taken by warp p % 8; each lane loads the S partials of its column
+          // for as many pieces as fit 16 values in flight, then sums each in
+          // split order
+          const int pieces = mine * 16;
+          auto reduce = [&](auto splits) {
+            constexpr int SS = decltype(splits)::value;
+            constexpr int B = 2 * kMaxSplits / SS;  // pieces per round: 16 values in flight
 #pragma unroll 1
-            for (int c = h; c < chunks; c += 2) {
-              float f[16];
+            for (int p0 = ew; p0 < pieces; p0 += kChainEpiWarps * B) {
+              float v[B][SS];
 #pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                f[e] = 0.0f;
-                if (16 * c + e < m_valid) {
-                  const float* src = part + static_cast<size_t>(16 * c + e) * kTileN + 32 * q + lane;
-                  f[e] = ld_cg_f32(src);
-                  for (int s2 = 1; s2 < L.splits; ++s2) f[e] += ld_cg_f32(src + static_cast<size_t>(s2) * BM * kTileN);
-                }
+              for (int bp = 0; bp < B; ++bp) {
+                const int piece = p0 + kChainEpiWarps * bp;
+                const int g = it.split + SS * (piece >> 4), row = 4 * g + ((piece & 15) >> 2), qq = piece & 3;
+                const bool in = piece < pieces && row < m_valid;
+#pragma unroll
+                for (int s2 = 0; s2 < SS; ++s2)
+                  v[bp][s2] = in ? __ldcg(part + (static_cast<size_t>(s2) * BM + row) * kTileN + 32 * qq + lane) : 0.0f;
               }
-              finish(f, c);
+#pragma unroll
+              for (int bp = 0; bp < B; ++bp) {
+                const int piece = p0 + kChainEpiWarps * bp;
+                const int g = it.split + SS * (piece >> 4), row = 4 * g + ((piece & 15) >> 2), qq = piece & 3;
+                float f = v[bp][0];
+#pragma unroll
+                for (int s2 = 1; s2 < SS; ++s2) f += v[bp][s2];
+                if (piece < pieces && row < m_valid) put(f, row, 32 * qq + lane);
+              }
             }
-            release();
+          };
+          switch (S) {
+            case 2: reduce(std::integral_constant<int, 2>{}); break;
+            case 3: reduce(std::integral_constant<int, 3>{}); break;
+            case 4: reduce(std::integral_constant<int, 4>{}); break;
+            case 5: reduce(std::integral_constant<int, 5>{}); break;
+            case 6: reduce(std::integral_constant<int, 6>{}); break;
+            case 7: reduce(std::integral_constant<int, 7>{}); break;
+            default: reduce(std::integral_constant<int, 8>{}); break;
           }
+          named_barrier(1, kChainEpiThreads);  // the staged rows are complete
+          if (mine > 0) write_rows(mine * 32, [&](int r) { return 4 * (it.split + S * (r >> 2)) + (r & 3); });
+          release();
         }
       }
     }

@@ -135,6 +135,7 @@ struct ChainLayerArgs {
   uint32_t* tickets;         // [tiles]: splits that have stored their partial
   int32_t N, K, k_tiles, kt_per_split, splits, n_tiles, items;
   int32_t in_n_tiles;        // N tiles of the layer producing this one's input (0: the first layer)
+  int32_t in_splits;         // K splits of that layer (each split CTA counts its share of a tile)
   int32_t k_tiles_next;
 };
 
@@ -154,7 +155,7 @@ struct ChainArgs {
   int32_t n_counters;
   int32_t layers, M, K0, k_tiles0, m_tiles, stages, a_box_rows;
   uint32_t tmem_cols;
-  uint32_t a_off, sfw_off, sfa_off, bar_off;
+  uint32_t a_off, sfw_off, sfa_off, epi_off, bar_off;
   int32_t weights_early;
 };
 

@@ -230,8 +230,9 @@ __device__ __forceinline__ uint32_t ld_after_wait_u8(const void* p) {
 // threads store their results, then each makes them visible at GPU scope
 // (fence_proxy_async_global for later TMA readers, then __threadfence), the
 // CTA synchronises, and one thread adds to the counter with release
-// semantics.  A consumer thread polls with acquire loads, then orders its own
-// later TMA reads after the acquire with fence_proxy_async_global.
+// semantics.  A consumer thread polls, orders its later accesses after the
+// observed value with an acquire fence, and its own later TMA reads after
+// that with fence_proxy_async_global.
 __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
   uint32_t v;
   asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -254,18 +255,33 @@ __device__ __forceinline__ void fence_proxy_async_global() {
   asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed_gpu(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
 // Waits until the counter equals `target` exactly, for at most timeout_ns of
-// global time; false if it gave up.  Equality, not >=: each counter receives
-// exactly its expected number of increments per launch, so a value past the
-// target means the counters did not start at zero (an uncleared workspace),
-// which then ends in a reported timeout instead of a wrong result.
+// global time; false if it gave up.  Polls with relaxed loads; once the value
+// is there, one acquire load of it orders the caller's later accesses.
+// Equality, not >=: each counter receives exactly its expected number of
+// increments per launch, so a value past the target means the counters did
+// not start at zero (an uncleared workspace), which then ends in a reported
+// timeout instead of a wrong result.
 __device__ __forceinline__ bool wait_count_eq(const uint32_t* p, uint32_t target, uint64_t timeout_ns) {
-  if (ld_acquire_gpu(p) == target) return true;
-  const uint64_t t0 = global_timer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (ld_acquire_gpu(p) == target) return true;
-    if ((it & 15u) == 0 && global_timer_ns() - t0 > timeout_ns) return false;
+  bool done = ld_relaxed_gpu(p) == target;
+  if (!done) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t it = 1;; ++it) {
+      if (ld_relaxed_gpu(p) == target) {
+        done = true;
+        break;
+      }
+      if ((it & 15u) == 0 && global_timer_ns() - t0 > timeout_ns) break;
+    }
   }
+  if (done) done = ld_acquire_gpu(p) == target;
+  return done;
 }
 
 __device__ __forceinline__ float ld_cg_f32(const float* p) {
