@@ -258,10 +258,11 @@ mxfp4_status_t prepare_gemm(const void* a, int64_t lda, const void* as, const vo
   g.stages = plan.stages;
   g.tmem_cols = static_cast<uint32_t>(plan.tmem_cols);
   g.timeout_ns = g_timeout_ns.load();
-  const GemmLayout GL = gemm_layout(plan.block_m, plan.stages, plan.splits, fused, M);
+  const GemmLayout GL = gemm_layout(plan.block_m, plan.stages, plan.splits, fused, M, abf_ring_for(plan, fused, M, dev->prop));
   g.a_off = GL.a_off;
   g.abf_off = GL.abf_off;
   g.abf_stage_bytes = GL.abf_stage;
+  g.abf_ring = GL.abf_ring;
   g.sfw_off = GL.sfw_off;
   g.sfa_off = GL.sfa_off;
   g.stg_off = GL.stg_off;

@@ -120,12 +120,17 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
   const int stages = args.stages;
+  // activation buffers: the fused kernel's bf16 staging ring (abf_ring
+  // buffers, tile i in buffer i % abf_ring, free again once quantized) is
+  // separate from the stages; the unfused kernel's codes land in the stages
+  const int nbuf = max(stages, args.abf_ring);
   auto full_w = [&](int s) { return sbase + args.bar_off + 8u * s; };                 // weight codes + scales
-  auto full_in = [&](int s) { return sbase + args.bar_off + 8u * (stages + s); };     // activation tile (TMA)
-  auto full_a = [&](int s) { return sbase + args.bar_off + 8u * (2 * stages + s); };  // operand ready for the MMA
-  auto empty = [&](int s) { return sbase + args.bar_off + 8u * (3 * stages + s); };   // stage consumed
-  const uint32_t accum_bar = sbase + args.bar_off + 8u * (4 * stages);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + args.bar_off + 8 * (4 * stages + 1));
+  auto full_a = [&](int s) { return sbase + args.bar_off + 8u * (stages + s); };      // operand ready for the MMA
+  auto empty = [&](int s) { return sbase + args.bar_off + 8u * (2 * stages + s); };   // stage consumed
+  auto full_in = [&](int r) { return sbase + args.bar_off + 8u * (3 * stages + r); }; // activation buffer (TMA)
+  auto abf_free = [&](int r) { return sbase + args.bar_off + 8u * (3 * stages + nbuf + r); };
+  const uint32_t accum_bar = sbase + args.bar_off + 8u * (3 * stages + 2 * nbuf);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + args.bar_off + 8 * (3 * stages + 2 * nbuf + 1));
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -145,9 +150,12 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_w(s), 1);
-      mbar_init(full_in(s), 1);
       mbar_init(full_a(s), C::kAWarps);  // one arrival per producer warp
       mbar_init(empty(s), 1);
+    }
+    for (int r = 0; r < nbuf; ++r) {
+      mbar_init(full_in(r), 1);
+      mbar_init(abf_free(r), C::kAWarps);
     }
     mbar_init(accum_bar, 1);
     *abort_flag = 0u;
@@ -197,6 +205,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         bulk_load(dst_sf, src_sf, kSfTileBytes, bar, policy_b);
       }
     };
+    // activation tile i: fused into bf16 staging buffer s = i % abf_ring,
+    // unfused into stage s
     auto issue_a = [&](int i, int s) {
       const int kt = kt_begin + i;
       const uint32_t bar = full_in(s);
@@ -233,26 +243,50 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     grid_dependency_wait();
     if (!args.weights_early)
       for (int i = 0; i < pre; ++i) issue_w(i, i);
-    for (int i = 0; i < pre; ++i) issue_a(i, i);
+    const int ring_a = kFused ? args.abf_ring : stages;  // activation buffers
+    const int pre_a = min(ring_a, kt_count);
+    for (int i = 0; i < pre_a; ++i) issue_a(i, i);
     if (args.trigger_late) grid_launch_dependents();
-    int issued = pre;
-    // (pre == stages whenever this loop runs: it starts over at stage 0, on the
-    // stages' second fill)
-    for (int i = pre, s = 0, round = 1; i < kt_count; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(empty(s), (round - 1) & 1, timeout))) {
-        if (leader) report_error(args.err, kErrWaitEmpty);
-        *abort_flag = 1u;
+    int issued_w = pre, issued_a = pre_a;
+    // refills: a stage's weights once its MMAs are done; an activation buffer
+    // once its tile is quantized (fused) or with its stage (unfused).  The
+    // ring and the stages differ in size, so a tile may need either or both.
+    for (int i = min(pre, pre_a); i < kt_count; ++i) {
+      bool ok = true;
+      if (i >= pre) {
+        const int s = i % stages, round = i / stages;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(empty(s), (round - 1) & 1, timeout));
+        if (!ok) {
+          if (leader) report_error(args.err, kErrWaitEmpty);
+          *abort_flag = 1u;
+        }
+        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+        issue_w(i, s);
+        issued_w = i + 1;
       }
-      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
-      issue_w(i, s);
-      issue_a(i, s);
-      issued = i + 1;
+      if (i < pre_a) continue;
+      if constexpr (kFused) {
+        const int r = i % ring_a, round_a = i / ring_a;
+        ok = __all_sync(0xFFFFFFFFu, mbar_wait(abf_free(r), (round_a - 1) & 1, timeout));
+        if (!ok) {
+          if (leader) report_error(args.err, kErrWaitEmpty);
+          *abort_flag = 1u;
+        }
+        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+        issue_a(i, r);
+      } else {
+        issue_a(i, i % stages);
+      }
+      issued_a = i + 1;
     }
     // Before the CTA can exit, every copy it issued must have landed.
-    for (int s = 0; s < stages && s < issued; ++s) {
-      const uint32_t parity = ((s + stages * ((issued - 1 - s) / stages)) / stages) & 1;
+    for (int s = 0; s < stages && s < issued_w; ++s) {
+      const uint32_t parity = ((s + stages * ((issued_w - 1 - s) / stages)) / stages) & 1;
       if (!mbar_wait(full_w(s), parity, timeout) && leader) report_error(args.err, kErrWaitDrain);
-      if (!mbar_wait(full_in(s), parity, timeout) && leader) report_error(args.err, kErrWaitDrain);
+    }
+    for (int r = 0; r < ring_a && r < issued_a; ++r) {
+      const uint32_t parity = ((r + ring_a * ((issued_a - 1 - r) / ring_a)) / ring_a) & 1;
+      if (!mbar_wait(full_in(r), parity, timeout) && leader) report_error(args.err, kErrWaitDrain);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -337,7 +371,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     uint32_t a_off = args.a_off, sfa_off = args.sfa_off, abf_off = args.abf_off;
     uint32_t abf_stage_bytes = args.abf_stage_bytes;
     int c_tma = args.c_tma;  // (for the epilogue)
-    asm volatile("" : "+r"(a_off), "+r"(sfa_off), "+r"(abf_off), "+r"(abf_stage_bytes), "+r"(c_tma));
+    int ring_a = kFused ? args.abf_ring : 1;
+    asm volatile("" : "+r"(a_off), "+r"(sfa_off), "+r"(abf_off), "+r"(abf_stage_bytes), "+r"(c_tma), "+r"(ring_a));
     bool triggered = !args.trigger_late;
     grid_dependency_wait();  // the activation (and C) may belong to the earlier grid
     const int64_t nblk = args.K / 32;
@@ -370,12 +405,14 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
           if (i < kt_count) load_scales(i, sc_pre[i][0], sc_pre[i][1]);
       }
     }
-    for (int i = 0, s = 0, round = 0; i < kt_count; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
+    for (int i = 0, s = 0, round = 0, r = 0, round_a = 0; i < kt_count;
+         ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0, r = r + 1 < ring_a ? r + 1 : 0, round_a += r == 0) {
       if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
         report_error(args.err, kErrWaitEmpty);
         *abort_flag = 1u;
       }
-      if (!*abort_flag && !mbar_wait(full_in(s), round & 1, timeout)) {
+      // fused: the tile's bf16 buffer r; unfused: the codes, in stage s
+      if (!*abort_flag && !mbar_wait(kFused ? full_in(r) : full_in(s), (kFused ? round_a : round) & 1, timeout)) {
         report_error(args.err, kErrWaitTma);
         *abort_flag = 1u;
       }
@@ -387,7 +424,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       uint8_t* a_tile = smem + a_off + s * C::kATileBytes;
       uint8_t* sfa = smem + sfa_off + s * C::kSfaStageBytes;
       if constexpr (kFused) {
-        const uint8_t* abf = smem + abf_off + s * abf_stage_bytes;
+        const uint8_t* abf = smem + abf_off + r * abf_stage_bytes;
         if (m_valid >= BM)
           quantize_tile<BM, C::kAThreads, C::kRowChunks, false>(abf, a_tile, sfa, tid, m_valid);
         else
@@ -416,7 +453,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       }
       fence_proxy_async_smem();  // make this thread's generic stores visible to tcgen05
       __syncwarp();              // ... and ordered before the warp's single arrival
-      if (lane == 0) mbar_arrive(full_a(s));
+      if (lane == 0) {
+        mbar_arrive(full_a(s));
+        if constexpr (kFused) mbar_arrive(abf_free(r));  // the bf16 buffer may be refilled
+      }
     }
 
     if (!triggered) grid_launch_dependents();
@@ -661,13 +701,14 @@ static uint32_t pow2_at_least(uint32_t x) {
   return p;
 }
 
-GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M) {
+GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M, int abf_ring) {
   GemmLayout L;
   const uint32_t st = static_cast<uint32_t>(stages), bm = static_cast<uint32_t>(block_m);
   L.a_off = st * kTileN * kTileKBytes;
   L.abf_off = L.a_off + st * bm * kTileKBytes;
   L.abf_stage = fused ? static_cast<uint32_t>(activation_box_rows(M, block_m)) * kTileK * 2 : 0u;
-  L.sfw_off = L.abf_off + st * L.abf_stage;
+  L.abf_ring = fused ? abf_ring : 0;
+  L.sfw_off = L.abf_off + static_cast<uint32_t>(L.abf_ring) * L.abf_stage;
   // without a K split the bf16 output tile is written over the operand
   // buffers once the MMAs are done: keep room for it before the scales
   if (splits == 1 && L.sfw_off < bm * kTileN * 2) L.sfw_off = bm * kTileN * 2;
@@ -677,8 +718,48 @@ GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t 
   const int blocks = static_cast<int>(4 * ceil_div(rows, 16));
   L.stg_blocks = splits > 1 ? static_cast<int32_t>(ceil_div(blocks, splits)) : 0;  // no split: no staging
   L.bar_off = L.stg_off + static_cast<uint32_t>(splits * L.stg_blocks) * kBlockBytes;
-  L.total = L.bar_off + (4 * st + 1) * 8 + 16;
+  const uint32_t nbuf = st > static_cast<uint32_t>(L.abf_ring) ? st : static_cast<uint32_t>(L.abf_ring);
+  L.total = L.bar_off + (3 * st + 2 * nbuf + 1) * 8 + 16;
   return L;
+}
+
+// Shared memory one CTA of plan p requests with a bf16 ring of `ring`
+// buffers; false if it exceeds the per-CTA limit.  Tensor-memory allocation
+// blocks while the SM's 512 columns are taken, and a blocked CTA of one
+// cluster could then wait on a CTA of another cluster that waits on it.  Each
+// CTA therefore takes shared memory in proportion to its tensor-memory share
+// (tmem_cols / 512 of the SM's shared memory): the CTAs that fit on an SM
+// together, from any mix of these kernels, can never ask for more than 512
+// columns, and no allocation ever waits.
+static bool plan_smem(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDeviceProp& prop, int ring,
+                      int64_t* bytes) {
+  const GemmLayout L = gemm_layout(p.block_m, p.stages, p.splits, fused, M, ring);
+  int64_t smem = static_cast<int64_t>(L.total) + 1024;  // + alignment slack
+  const int64_t per_sm = prop.sharedMemPerMultiprocessor;
+  const int64_t reserved = prop.reservedSharedMemPerBlock;
+  const int64_t floor_smem = (per_sm * p.tmem_cols + 511) / 512 - reserved;
+  if (smem < floor_smem) smem = floor_smem;
+  smem = (smem + 15) / 16 * 16;
+  *bytes = smem;
+  return smem <= static_cast<int64_t>(prop.sharedMemPerBlockOptin);
+}
+
+int abf_ring_for(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDeviceProp& prop) {
+  if (!fused) return 0;
+  // as many bf16 buffers as the split has K tiles (all in flight at once), up
+  // to kAbfRing, as long as the CTA still fits -- and still shares an SM with
+  // another CTA when it would with a single buffer
+  auto two_per_sm = [&](int64_t smem) {
+    return 2 * (smem + static_cast<int64_t>(prop.reservedSharedMemPerBlock)) <=
+           static_cast<int64_t>(prop.sharedMemPerMultiprocessor);
+  };
+  int64_t one = 0;
+  const bool fits1 = plan_smem(p, fused, M, prop, 1, &one);
+  for (int r = p.k_tiles_per_split < kAbfRing ? p.k_tiles_per_split : kAbfRing; r > 1; --r) {
+    int64_t b = 0;
+    if (plan_smem(p, fused, M, prop, r, &b) && (!fits1 || !two_per_sm(one) || two_per_sm(b))) return r;
+  }
+  return 1;
 }
 
 bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
@@ -705,20 +786,8 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
   const uint32_t tcols = pow2_at_least(p->accumulators * p->block_m + p->stages * sf_cols_for(p->block_m));
   if (tcols > 512) return false;
   p->tmem_cols = static_cast<int32_t>(tcols);
-  const GemmLayout L = gemm_layout(p->block_m, p->stages, p->splits, fused, M);
-  int64_t smem = static_cast<int64_t>(L.total) + 1024;  // + alignment slack
-  // Tensor-memory allocation blocks while the SM's 512 columns are taken, and
-  // a blocked CTA of one cluster could then wait on a CTA of another cluster
-  // that waits on it.  Each CTA therefore takes shared memory in proportion to
-  // its tensor-memory share (tmem_cols / 512 of the SM's shared memory): the
-  // CTAs that fit on an SM together, from any mix of these kernels, can never
-  // ask for more than 512 columns, and no allocation ever waits.
-  const int64_t per_sm = prop.sharedMemPerMultiprocessor;
-  const int64_t reserved = prop.reservedSharedMemPerBlock;
-  const int64_t floor_smem = (per_sm * tcols + 511) / 512 - reserved;
-  if (smem < floor_smem) smem = floor_smem;
-  smem = (smem + 15) / 16 * 16;
-  if (smem > static_cast<int64_t>(prop.sharedMemPerBlockOptin)) return false;
+  int64_t smem = 0;
+  if (!plan_smem(*p, fused, M, prop, abf_ring_for(*p, fused, M, prop), &smem)) return false;
   p->smem_bytes = static_cast<int32_t>(smem);
   return true;
 }
@@ -787,7 +856,9 @@ struct TunedPlan {
   int block_m, splits, stages;
 };
 constexpr TunedPlan kTunedPlans[] = {
-    {16, 2112, 7168, true, 16, 7, 3},
+    {16, 2112, 7168, true, 16, 7, 4},
+    {8, 2112, 7168, true, 16, 7, 4},
+    {16, 3072, 1536, true, 16, 2, 3},
     {64, 7168, 2048, false, 64, 2, 4},
     {256, 3072, 1536, false, 64, 1, 6},
 };
@@ -803,7 +874,7 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
                   mxfp4_plan_t* p) {
   *p = mxfp4_plan_t{};
   // A tuned plan is keyed on the shape; it is taken on any device where it
-  // still fits and runs in one wave (every cluster resident at once).
+  // fits and its CTAs are at most two per SM.
   for (const TunedPlan& t : kTunedPlans) {
     if (t.M != M || t.N != N || t.K != K || t.fused != fused) continue;
     mxfp4_plan_t q{};
@@ -811,9 +882,8 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
     q.splits = t.splits;
     q.stages = t.stages;
     if (!finish_plan(M, N, K, fused, prop, &q)) continue;
-    const int64_t clusters = static_cast<int64_t>(q.grid_y) * q.grid_z;
-    if (clusters * q.splits <= 2 * static_cast<int64_t>(prop.multiProcessorCount) &&
-        clusters <= active_clusters(q, fused)) {
+    const int64_t ctas = static_cast<int64_t>(q.grid_y) * q.grid_z * q.splits;
+    if (ctas <= 2 * static_cast<int64_t>(prop.multiProcessorCount)) {
       *p = q;
       return;
     }

@@ -69,11 +69,18 @@ struct GemmArgs {
   int32_t accumulators;     // independent fp32 accumulator tiles in tensor memory (1, 2, 4)
   int32_t c_tma;            // no K split: C leaves through a bf16 tile in shared memory and one TMA store
   int32_t trigger_late;     // let the next grid launch only once this grid has passed its own wait
+  int32_t abf_ring;         // fused: bf16 staging buffers (a ring of its own, at most kAbfRing)
 };
+
+// bf16 activation buffers of the fused kernel: tile i is staged in buffer
+// i % ring and the buffer is refilled once that tile is quantized, so the
+// stage count (weight tiles in flight) does not pay for bf16 staging; the
+// ring holds all of a split's K tiles up to this many.
+constexpr int kAbfRing = 4;
 
 // Shared-memory layout of one GEMM CTA (byte offsets from a 1024-aligned base):
 // weight code tiles, activation code tiles, bf16 activation staging (fused,
-// activation_box_rows x 512 bytes per stage),
+// activation_box_rows x 512 bytes per buffer, min(K tiles per split, kAbfRing) buffers),
 // weight scales, activation scales (one of each per stage), the split-K
 // staging slots ([splits][stg_blocks] blocks of 2 KB), then the mbarriers.
 // Without a K split the bf16 output tile [block_m][128] is staged at offset 0
@@ -88,10 +95,13 @@ inline int activation_box_rows(int64_t M, int block_m) {
 
 struct GemmLayout {
   uint32_t a_off, abf_off, sfw_off, sfa_off, stg_off, bar_off, total;
-  uint32_t abf_stage;  // bf16 staging bytes per stage (fused)
+  uint32_t abf_stage;  // bf16 staging bytes per buffer (fused)
+  int32_t abf_ring;    // bf16 staging buffers (fused)
   int32_t stg_blocks;
 };
-GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M);
+GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M, int abf_ring);
+// The fused kernel's bf16 buffer count for a finished plan (0 unfused).
+int abf_ring_for(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDeviceProp& prop);
 
 // Launchers (return a CUDA error code; arguments are validated by the caller).
 cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, void* Aq, void* As,
