@@ -237,6 +237,70 @@ class Chain:
         return g
 
 
+class MultiLayer:
+    """The same chain of layers as Chain, run through the multi-layer entry
+    (mxfp4_quant_gemm_chain): launches of `per_launch` layers each, launch j's
+    input the previous launch's last output."""
+
+    def __init__(self, chain: Chain, per_launch: int = 16):
+        mx, w = chain.mx, chain.w
+        self.chain, self.mx = chain, mx
+        L = chain.layers
+        self.groups = [L[i:i + per_launch] for i in range(0, len(L) - len(L) % per_launch, per_launch)]
+        Ns = [W.N for W in self.groups[0]]
+        dev = chain.x.device
+        self.outs = [torch.empty((w.M, n), dtype=torch.bfloat16, device=dev) for n in Ns]
+        self.ws = torch.zeros(mx.chain_workspace_bytes(w.M, w.K, Ns), dtype=torch.uint8, device=dev)
+        self.layers = per_launch * len(self.groups)
+
+    def calls(self, stream):
+        return [self.mx.prepare_quant_gemm_chain(self.chain.x if j == 0 else self.outs[-1], g, outs=self.outs,
+                                                 workspace=self.ws, stream=stream)
+                for j, g in enumerate(self.groups)]
+
+
+def time_multilayer(ml: MultiLayer, stream: torch.cuda.Stream, reps: int = 3) -> tuple[float, float]:
+    """(µs per layer graph-replayed, µs per layer with every launch issued from
+    the host) of the multi-layer entry."""
+    calls = ml.calls(stream)
+    for c in calls:
+        c()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        with torch.cuda.graph(g, stream=stream):
+            for c in calls:
+                c()
+    with torch.cuda.stream(stream):
+        g.replay()
+    torch.cuda.synchronize()
+    graphed = float(np.median([_timed(g.replay, ml.chain.flush, stream) for _ in range(reps)])) * 1e3 / ml.layers
+
+    def eager():
+        for c in calls:
+            c()
+
+    eager_us = float(np.median([_timed(eager, ml.chain.flush, stream) for _ in range(reps)])) * 1e3 / ml.layers
+    return graphed, eager_us
+
+
+def time_chain_eager(chain: Chain, stream: torch.cuda.Stream, reps: int = 3) -> float:
+    """µs per layer of the dependent chain with every per-layer call issued from
+    the host (prepared calls, no graph)."""
+    calls = []
+    for i, W in enumerate(chain.layers):
+        src, dst = (chain.x, chain.y) if i % 2 == 0 else (chain.y, chain.x)
+        calls.append(chain.mx.prepare_quant_gemm(src, W, out=dst, workspace=chain.ws, stream=stream))
+
+    def eager():
+        for c in calls:
+            c()
+
+    eager()
+    torch.cuda.synchronize()
+    return float(np.median([_timed(eager, chain.flush, stream) for _ in range(reps)])) * 1e3 / len(calls)
+
+
 def aggregate_over_ranks(ms_local: float, steps: int, world: int) -> tuple[float, float]:
     """The job's time is the slowest rank's (all_reduce MAX over the process
     group when world > 1); the whole-job value is that time per call over all
@@ -451,7 +515,15 @@ def latency_report(w: workloads.Workload, prob: Problem, stream: torch.cuda.Stre
         out["chain_layers"] = len(chain.layers)
         out["chain_how"] = (f"a CUDA graph of {len(chain.layers)} dependent layers alternating [M,K]->[M,N] and "
                             f"[M,N]->[M,K], each with its own weight copy; µs per layer")
-        del chain
+        out["chain_eager_us_per_layer"] = round(time_chain_eager(chain, stream), 4)
+        ml = MultiLayer(chain)
+        graphed, eager = time_multilayer(ml, stream)
+        out["multilayer_us_per_layer"] = round(graphed, 4)
+        out["multilayer_eager_us_per_layer"] = round(eager, 4)
+        out["multilayer_how"] = (f"the same layers through mxfp4_quant_gemm_chain, {len(ml.groups)} launches of "
+                                 f"{len(ml.groups[0])} layers; graph-replayed, and issued from the host per launch "
+                                 f"(the eager figure beside chain_eager_us_per_layer: one host call per layer)")
+        del chain, ml
     finally:
         mx.set_programmatic_launch(3)
     return out
@@ -555,7 +627,9 @@ def run_ours(args) -> dict:
         out["per_shape"] = shapes
         head = shapes[name]
         out["latency"] = {k: head[k] for k in ("us_per_call_no_overlap", "chain_us_per_layer",
-                                               "chain_us_per_layer_no_overlap") if k in head}
+                                               "chain_us_per_layer_no_overlap", "chain_eager_us_per_layer",
+                                               "multilayer_us_per_layer", "multilayer_eager_us_per_layer")
+                          if k in head}
         err = mx.device_error(reset=True)
         if err:
             raise RuntimeError(f"device error word {err:#x} after the per-shape timings")
@@ -569,6 +643,24 @@ def run_ours(args) -> dict:
 
         dist.destroy_process_group()
     return out if rank == 0 else None
+
+
+def run_multilayer_only(args) -> dict:
+    """The multi-layer entry alone on the workload's chain of up/down layers
+    (graph-replayed and host-issued µs per layer); no headline line."""
+    import block_scaled_mxfp4_activation_gb300 as mx
+
+    torch.cuda.set_device(0)
+    mx.load_library()
+    stream = torch.cuda.Stream()
+    w = ALL_WORKLOADS[args.workload]
+    ml = MultiLayer(Chain(w, torch.device("cuda", 0)))
+    graphed, eager = time_multilayer(ml, stream)
+    err = mx.device_error(reset=True)
+    if err:
+        raise RuntimeError(f"device error word {err:#x}")
+    return {"workload": args.workload, "layers": ml.layers, "multilayer_us_per_layer": round(graphed, 4),
+            "multilayer_eager_us_per_layer": round(eager, 4)}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -628,8 +720,13 @@ def main(argv=None):
     ap.add_argument("--all-shapes", dest="all_shapes", action="store_true", default=True)
     ap.add_argument("--headline-only", dest="all_shapes", action="store_false")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--multilayer-only", action="store_true",
+                    help="time only the multi-layer entry on the workload's up/down chain (a profiling target)")
     args = ap.parse_args(argv)
-    out = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if args.multilayer_only:
+        out = run_multilayer_only(args)
+    else:
+        out = run_reference(args) if args.impl == "reference" else run_ours(args)
     if out is not None:
         print(json.dumps(out), flush=True)
 

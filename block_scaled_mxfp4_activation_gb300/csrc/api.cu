@@ -89,7 +89,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 // promotion 256 B, no OOB fill), reusing the result of an identical earlier
 // request from this thread: a map holds only the address, shape, strides and
 // box, so repeated calls on the same buffers (every layer call, every step of
-// a loop) skip the encoder.  A small round-robin cache per thread.
+// a loop) skip the encoder.  A direct-mapped cache per thread: one hashed slot
+// per request, so a lookup is one comparison whether it hits or misses.
 bool encode_2d(CUtensorMapDataType type, const void* base, uint64_t dim0, uint64_t dim1, uint64_t stride1,
                uint32_t box0, uint32_t box1, CUtensorMapSwizzle swizzle, CUtensorMap* map) {
   struct Entry {
@@ -100,16 +101,17 @@ bool encode_2d(CUtensorMapDataType type, const void* base, uint64_t dim0, uint64
     bool valid;
     CUtensorMap map;
   };
-  constexpr int kEntries = 64;  // room for a multi-layer launch's maps
-  thread_local Entry cache[kEntries] = {};
-  thread_local int next = 0;
-  for (int i = 0; i < kEntries; ++i) {
-    const Entry& e = cache[i];
-    if (e.valid && e.base == base && e.dim0 == dim0 && e.dim1 == dim1 && e.stride1 == stride1 && e.box0 == box0 &&
-        e.box1 == box1 && e.type == static_cast<int>(type) && e.swizzle == static_cast<int>(swizzle)) {
-      *map = e.map;
-      return true;
-    }
+  constexpr int kSlots = 256;
+  thread_local Entry cache[kSlots] = {};
+  uint64_t h = reinterpret_cast<uintptr_t>(base) * 0x9E3779B97F4A7C15ull;
+  h ^= (dim0 * 0xC2B2AE3D27D4EB4Full) ^ (dim1 * 0x165667B19E3779F9ull) ^ (stride1 << 7) ^
+       (static_cast<uint64_t>(box0) << 17) ^ (static_cast<uint64_t>(box1) << 29) ^
+       (static_cast<uint64_t>(type) << 41) ^ (static_cast<uint64_t>(swizzle) << 47);
+  Entry& e = cache[(h ^ (h >> 29)) & (kSlots - 1)];
+  if (e.valid && e.base == base && e.dim0 == dim0 && e.dim1 == dim1 && e.stride1 == stride1 && e.box0 == box0 &&
+      e.box1 == box1 && e.type == static_cast<int>(type) && e.swizzle == static_cast<int>(swizzle)) {
+    *map = e.map;
+    return true;
   }
   auto encode = tensor_map_encoder();
   if (encode == nullptr) return false;
@@ -120,8 +122,6 @@ bool encode_2d(CUtensorMapDataType type, const void* base, uint64_t dim0, uint64
   if (encode(map, type, 2, const_cast<void*>(base), dims, strides, box, elem_strides, CU_TENSOR_MAP_INTERLEAVE_NONE,
              swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
     return false;
-  Entry& e = cache[next];
-  next = (next + 1) % kEntries;
   e = Entry{base, dim0, dim1, stride1, box0, box1, static_cast<int>(type), static_cast<int>(swizzle), true, *map};
   return true;
 }
