@@ -48,7 +48,7 @@ class MXFP4Error(RuntimeError):
 class Plan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "block_m", "splits", "stages", "k_tiles_per_split", "grid_x", "grid_y", "grid_z", "threads",
-        "smem_bytes", "tmem_cols", "two_pass", "accumulators")]
+        "smem_bytes", "tmem_cols", "two_pass", "accumulators", "share")]
 
     def as_dict(self) -> dict:
         return {n: getattr(self, n) for n, _ in self._fields_}
@@ -426,7 +426,8 @@ def gemm_plan(M: int, N: int, K: int, fused: bool = True) -> dict:
 
 def gemm_with_plan(A_or_Aq: torch.Tensor, As: torch.Tensor | None, W: PackedWeight, plan: dict,
                    fused: bool, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
-    """Either GEMM entry with an explicit tile plan (block_m, splits, stages)."""
+    """Either GEMM entry with an explicit tile plan (block_m, splits, stages, and
+    optionally accumulators and share)."""
     W = _weight(W)
     M = A_or_Aq.shape[0]
     if fused:
@@ -441,6 +442,7 @@ def gemm_with_plan(A_or_Aq: torch.Tensor, As: torch.Tensor | None, W: PackedWeig
     p = Plan()
     p.block_m, p.splits, p.stages = int(plan["block_m"]), int(plan["splits"]), int(plan.get("stages", 0))
     p.accumulators = int(plan.get("accumulators", 0))
+    p.share = int(plan.get("share", 0))
     _call("mxfp4_gemm_with_plan", _ptr(A_or_Aq), lda, _ptr(As), _ptr(W.data), _ptr(out), M, W.N, W.K,
           int(fused), ctypes.byref(p), _stream(stream))
     return out

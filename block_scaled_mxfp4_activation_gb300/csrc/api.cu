@@ -228,6 +228,7 @@ mxfp4_status_t prepare_gemm(const void* a, int64_t lda, const void* as, const vo
     plan.splits = user_plan->splits;
     plan.stages = user_plan->stages;
     plan.accumulators = user_plan->accumulators;
+    plan.share = user_plan->share;
     if (!finish_plan(M, N, K, fused, dev->prop, &plan)) return MXFP4_ERR_INVALID_ARG;
   } else {
     cached_default_plan(M, N, K, fused, dev->prop, &plan);
@@ -263,6 +264,7 @@ mxfp4_status_t prepare_gemm(const void* a, int64_t lda, const void* as, const vo
   g.abf_off = GL.abf_off;
   g.abf_stage_bytes = GL.abf_stage;
   g.abf_ring = GL.abf_ring;
+  g.share = fused ? plan.share : 1;
   g.sfw_off = GL.sfw_off;
   g.sfa_off = GL.sfa_off;
   g.stg_off = GL.stg_off;

@@ -109,9 +109,73 @@ __device__ __forceinline__ void quantize_tile(const uint8_t* abf, uint8_t* a_til
   }
 }
 
+// The same quantization for a tile shared along N: the tile's codes and the
+// scale words of its rows go to the same stage of every CTA that shares it
+// (`share` CTAs, cluster ranks rank0 + rank_step * t), by st.async completing
+// on that CTA's full_a barrier of the stage -- the receiver waits for
+// rows_valid x 136 bytes (128 of codes, two 4-byte scale words).  A scale word
+// holds the four blocks of one 128-wide chunk of a row: in a half-warp (one
+// row), lanes 8c + 2j hold block 4c + j, gathered by four shuffles.
+template <int BM, int kThreads, int kRowChunks>
+__device__ __forceinline__ void quantize_tile_push(const uint8_t* abf, uint32_t a_tile_s, uint32_t sfa_s,
+                                                   uint32_t bar_s, int tid, int rows_valid, int share,
+                                                   uint32_t rank0, uint32_t rank_step) {
+  constexpr int kUnits = BM * 16 / kThreads;
+  const int lane = tid & 31, pw = tid >> 5;
+  const int rot = (lane >> 2) & 1;
+  const int half = lane & 1;
+  constexpr int kBatch = kUnits < (BM < 128 ? 4 : 2) ? kUnits : (BM < 128 ? 4 : 2);
+#pragma unroll(BM < 256 ? kUnits / kBatch : 1)
+  for (int k0 = 0; k0 < kUnits; k0 += kBatch) {
+    uint4 v[kBatch][2];
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      const uint8_t* src = abf + (tid + (k0 + e) * kThreads) * 32;
+      if (2 * pw + 16 * (k0 + e) < rows_valid) {
+        v[e][0] = *reinterpret_cast<const uint4*>(src + 16 * rot);
+        v[e][1] = *reinterpret_cast<const uint4*>(src + 16 * (rot ^ 1));
+      }
+    }
+#pragma unroll
+    for (int e = 0; e < kBatch; ++e) {
+      if (2 * pw + 16 * (k0 + e) >= rows_valid) continue;  // warp-uniform (rows come in pairs)
+      const int u = tid + (k0 + e) * kThreads;
+      const int m = u >> 4, b = (u >> 1) & 7;
+      uint32_t amax = absmax16_bf16(v[e][0], v[e][1]);
+      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      const uint32_t byte = scale_byte_from_amax(amax);
+      const uint16_t sbf = scale_bf16_from_byte(byte);
+      uint32_t w0 = e2m1_pack8(v[e][0], sbf), w1 = e2m1_pack8(v[e][1], sbf);
+      if (rot) {
+        const uint32_t t = w0;
+        w0 = w1;
+        w1 = t;
+      }
+      const int base = lane & ~7;
+      const uint32_t word = __shfl_sync(0xFFFFFFFFu, byte, base) | (__shfl_sync(0xFFFFFFFFu, byte, base + 2) << 8) |
+                            (__shfl_sync(0xFFFFFFFFu, byte, base + 4) << 16) |
+                            (__shfl_sync(0xFFFFFFFFu, byte, base + 6) << 24);
+      const uint32_t code_off = a_tile_s + m * kTileKBytes + ((b ^ (m & 7)) << 4) + 8 * half;
+      const uint32_t sf_off = sfa_s + ((b >> 2) * kRowChunks + (m >> 7)) * kSfChunkBytes + sf_chunk_offset(m);
+      for (int t = 0; t < share; ++t) {
+        const uint32_t r = rank0 + rank_step * static_cast<uint32_t>(t);
+        const uint32_t cbar = map_to_rank(bar_s, r);
+        st_async_v2(map_to_rank(code_off, r), w0, w1, cbar);
+        if ((lane & 7) == 0) st_async_b32(map_to_rank(sf_off, r), word, cbar);
+      }
+    }
+  }
+}
+
 // kHostC: every element of C is also written to args.c_host (mapped host
 // memory); a separate instantiation, so the common kernels carry none of it.
-template <int BM, bool kFused, bool kHostC>
+// kShare (fused only): the args.share CTAs of a cluster that hold neighbouring
+// N tiles of the same rows and K split quantize the split's K tiles between
+// them -- tile i by the CTA of share rank i % share -- and push each tile's
+// codes and scales into all of their operand buffers (quantize_tile_push).
+// The cluster is splits x share; every stage holds its own K tile (stages ==
+// K tiles per split), so nothing is refilled.
+template <int BM, bool kFused, bool kHostC, bool kShare>
 __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
@@ -135,7 +199,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int splits = args.splits;
-  const uint32_t rank = splits > 1 ? cluster_ctarank() : 0u;
+  // K split of this CTA = its x in the cluster; with kShare, its share rank is y
+  const uint32_t rank = (splits > 1 || kShare) ? cluster_ctaid_x() : 0u;
+  const uint32_t share_rank = kShare ? cluster_ctaid_y() : 0u;
+  const int share = kShare ? args.share : 1;
   const int n_tile = blockIdx.y, m_tile = blockIdx.z;
   const int m_base = m_tile * BM;
   const int m_valid = min(BM, args.M - m_base);
@@ -150,8 +217,19 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_w(s), 1);
-      mbar_init(full_a(s), C::kAWarps);  // one arrival per producer warp
+      mbar_init(full_a(s), kShare ? 1 : C::kAWarps);  // one arrival per producer warp; kShare: own arrival + bytes
       mbar_init(empty(s), 1);
+    }
+    if constexpr (kShare) {
+      // every stage's operand arrives from the CTA that quantizes its K tile:
+      // arm each with the bytes it will receive (a_box_rows x 136)
+      for (int s = 0; s < kt_count && s < stages; ++s)
+        mbar_arrive_expect_tx(full_a(s), args.a_box_rows * (kTileKBytes + 8));
+      // (the host gives a shared plan a stage per K tile and a bf16 buffer per own tile)
+      if (kt_count > stages || (kt_count + args.share - 1) / args.share > args.abf_ring) {
+        report_error(args.err, kErrBadPlan);
+        *abort_flag = 1u;
+      }
     }
     for (int r = 0; r < nbuf; ++r) {
       mbar_init(full_in(r), 1);
@@ -172,6 +250,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   }
   tc_fence_before_sync();
   __syncthreads();
+  // kShare: peers push into this CTA's buffers and barriers only after every
+  // CTA of the cluster has initialised its barriers
+  if constexpr (kShare) cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const int nacc = args.accumulators;                 // independent accumulators (1, 2 or 4)
@@ -244,14 +325,21 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     if (!args.weights_early)
       for (int i = 0; i < pre; ++i) issue_w(i, i);
     const int ring_a = kFused ? args.abf_ring : stages;  // activation buffers
-    const int pre_a = min(ring_a, kt_count);
-    for (int i = 0; i < pre_a; ++i) issue_a(i, i);
+    // kShare: this CTA loads (and quantizes) only K tiles share_rank, + share, ...
+    const int own = kShare ? (kt_count - static_cast<int>(share_rank) + share - 1) / share : kt_count;
+    const int pre_a = min(ring_a, own);
+    if constexpr (kShare) {
+      for (int j = 0; j < pre_a; ++j) issue_a(static_cast<int>(share_rank) + j * share, j);
+    } else {
+      for (int i = 0; i < pre_a; ++i) issue_a(i, i);
+    }
     if (args.trigger_late) grid_launch_dependents();
     int issued_w = pre, issued_a = pre_a;
     // refills: a stage's weights once its MMAs are done; an activation buffer
     // once its tile is quantized (fused) or with its stage (unfused).  The
     // ring and the stages differ in size, so a tile may need either or both.
-    for (int i = min(pre, pre_a); i < kt_count; ++i) {
+    // (kShare: the ring holds every own tile and the stages every tile.)
+    for (int i = kShare ? kt_count : min(pre, pre_a); i < kt_count; ++i) {
       bool ok = true;
       if (i >= pre) {
         const int s = i % stages, round = i / stages;
@@ -405,7 +493,29 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
           if (i < kt_count) load_scales(i, sc_pre[i][0], sc_pre[i][1]);
       }
     }
-    for (int i = 0, s = 0, round = 0, r = 0, round_a = 0; i < kt_count;
+    if constexpr (kShare) {
+      // quantize this CTA's own K tiles, each into the same stage of every
+      // CTA sharing it; the MMA warps wait on their own barriers
+      const int own = (kt_count - static_cast<int>(share_rank) + share - 1) / share;
+      const uint32_t rank0 = rank;  // share rank t is cluster rank rank + splits * t
+      for (int j = 0; j < own; ++j) {
+        const int i = static_cast<int>(share_rank) + j * share;
+        if (!*abort_flag && !mbar_wait(full_in(j), 0, timeout)) {
+          report_error(args.err, kErrWaitTma);
+          *abort_flag = 1u;
+        }
+        if (!triggered) {  // the activation tile has landed: the next grid may start
+          grid_launch_dependents();
+          triggered = true;
+        }
+        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+        quantize_tile_push<BM, C::kAThreads, C::kRowChunks>(
+            smem + abf_off + j * abf_stage_bytes, sbase + a_off + i * C::kATileBytes,
+            sbase + sfa_off + i * C::kSfaStageBytes, full_a(i), tid, args.a_box_rows, share, rank0,
+            static_cast<uint32_t>(splits));
+      }
+    }
+    for (int i = 0, s = 0, round = 0, r = 0, round_a = 0; !kShare && i < kt_count;
          ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0, r = r + 1 < ring_a ? r + 1 : 0, round_a += r == 0) {
       if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
         report_error(args.err, kErrWaitEmpty);
@@ -553,7 +663,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         for (int e = 0; e < 16; ++e)
           *reinterpret_cast<float*>(smem + (dst - sbase) + e * 128) = __uint_as_float(r[e]);
       } else {
-        const uint32_t cdst = map_to_rank(dst, owner);
+        const uint32_t cdst = map_to_rank(dst, owner + static_cast<uint32_t>(splits) * share_rank);
 #pragma unroll
         for (int e = 0; e < 16; ++e) st_cluster_f32(cdst + e * 128, __uint_as_float(r[e]));
       }
@@ -589,7 +699,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   uint32_t stg_stride = static_cast<uint32_t>(args.stg_blocks) * kBlockBytes;
   asm volatile("" : "+r"(n_cols), "+l"(c_out), "+r"(stg_stride));
   tc_fence_before_sync();
-  if (splits > 1) cluster_sync_all(); else __syncthreads();
+  if (splits > 1 || kShare) cluster_sync_all(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, args.tmem_cols);
@@ -640,17 +750,21 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
 }
 
 // ----------------------------------------------------------------------------- host side
-template <int BM, bool kFused, bool kHostC>
+template <int BM, bool kFused, bool kHostC, bool kShare>
 static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                             const GemmArgs& args, const mxfp4_plan_t& plan, bool programmatic, cudaStream_t s) {
-  auto kernel = mxfp4_gemm_kernel<BM, kFused, kHostC>;
-  static int configured_device = -1;  // max dynamic smem set once per device
+  auto kernel = mxfp4_gemm_kernel<BM, kFused, kHostC, kShare>;
+  static int configured_device = -1;  // max dynamic smem (and cluster size) set once per device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (configured_device != dev) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
     if (e != cudaSuccess) return e;
+    if (kShare) {  // splits x share may exceed the portable 8
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+      if (e != cudaSuccess) return e;
+    }
     configured_device = dev;
   }
   cudaLaunchConfig_t cfg = {};
@@ -661,7 +775,7 @@ static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = plan.splits;
-  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.y = kShare ? plan.share : 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = programmatic ? 1 : 0;
@@ -673,13 +787,26 @@ static cudaError_t launch_t(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a
 cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, const CUtensorMap& tmap_c,
                         const GemmArgs& args, const mxfp4_plan_t& plan, bool fused, bool programmatic,
                         cudaStream_t s) {
-#define MXFP4_LAUNCH(BM_)                                                                           \
-  case BM_:                                                                                         \
-    if (args.c_host != nullptr)                                                                     \
-      return fused ? launch_t<BM_, true, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s) \
-                   : launch_t<BM_, false, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s); \
-    return fused ? launch_t<BM_, true, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s)  \
-                 : launch_t<BM_, false, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);
+#define MXFP4_LAUNCH(BM_)                                                                                   \
+  case BM_:                                                                                                 \
+    if (args.c_host != nullptr)                                                                             \
+      return fused ? launch_t<BM_, true, true, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s)  \
+                   : launch_t<BM_, false, true, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s); \
+    return fused ? launch_t<BM_, true, false, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s)   \
+                 : launch_t<BM_, false, false, false>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);
+#define MXFP4_LAUNCH_SHARE(BM_)                                                                         \
+  case BM_:                                                                                             \
+    if (args.c_host != nullptr)                                                                         \
+      return launch_t<BM_, true, true, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);      \
+    return launch_t<BM_, true, false, true>(tmap_b, tmap_a, tmap_c, args, plan, programmatic, s);
+  if (fused && plan.share > 1) {
+    switch (plan.block_m) {  // quantization shared along N: block_m up to 64
+      MXFP4_LAUNCH_SHARE(16)
+      MXFP4_LAUNCH_SHARE(32)
+      MXFP4_LAUNCH_SHARE(64)
+      default: return cudaErrorInvalidValue;
+    }
+  }
   switch (plan.block_m) {
     MXFP4_LAUNCH(16)
     MXFP4_LAUNCH(32)
@@ -688,6 +815,7 @@ cudaError_t launch_gemm(const CUtensorMap& tmap_b, const CUtensorMap& tmap_a, co
     MXFP4_LAUNCH(256)
     default: return cudaErrorInvalidValue;
   }
+#undef MXFP4_LAUNCH_SHARE
 #undef MXFP4_LAUNCH
 }
 
@@ -746,6 +874,7 @@ static bool plan_smem(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDe
 
 int abf_ring_for(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDeviceProp& prop) {
   if (!fused) return 0;
+  if (p.share > 1) return (p.k_tiles_per_split + p.share - 1) / p.share;  // every own tile in flight
   // as many bf16 buffers as the split has K tiles (all in flight at once), up
   // to kAbfRing, as long as the CTA still fits -- and still shares an SM with
   // another CTA when it would with a single buffer
@@ -773,6 +902,16 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
   if ((p->splits - 1) * per >= k_tiles) return false;
   if (p->stages < 1 || p->stages > per) p->stages = static_cast<int32_t>(per < 6 ? per : 6);
   p->k_tiles_per_split = static_cast<int32_t>(per);
+  // quantization shared along N: fused, block_m <= 64, share divides the N
+  // tiles, a cluster of splits x share <= 16, and a stage per K tile
+  if (p->share == 0) p->share = 1;
+  if (p->share < 1) return false;
+  if (p->share > 1) {
+    if (!fused || p->block_m > 64 || ceil_div(N, kTileN) % p->share != 0 || p->splits * p->share > 16 ||
+        p->share > per)
+      return false;
+    p->stages = static_cast<int32_t>(per);
+  }
   p->grid_x = p->splits;
   p->grid_y = static_cast<int32_t>(ceil_div(N, kTileN));
   p->grid_z = static_cast<int32_t>(ceil_div(M, p->block_m));
@@ -792,10 +931,11 @@ bool finish_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDevicePr
   return true;
 }
 
-template <int BM, bool kFused>
+template <int BM, bool kFused, bool kShare>
 static int active_clusters_t(const mxfp4_plan_t& p) {
-  auto kernel = mxfp4_gemm_kernel<BM, kFused, false>;  // the host-copy kernels use the same resources
+  auto kernel = mxfp4_gemm_kernel<BM, kFused, false, kShare>;  // the host-copy kernels use the same resources
   if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024) != cudaSuccess) return 0;
+  if (kShare && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess) return 0;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.grid_x, p.grid_y, p.grid_z);
   cfg.blockDim = dim3(p.threads, 1, 1);
@@ -803,7 +943,7 @@ static int active_clusters_t(const mxfp4_plan_t& p) {
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = p.splits;
-  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.y = kShare ? p.share : 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
@@ -817,8 +957,16 @@ static int active_clusters_t(const mxfp4_plan_t& p) {
 
 // How many clusters of this plan can be resident at once on the device.
 static int active_clusters(const mxfp4_plan_t& p, bool fused) {
+  if (fused && p.share > 1) {
+    switch (p.block_m) {
+      case 16: return active_clusters_t<16, true, true>(p);
+      case 32: return active_clusters_t<32, true, true>(p);
+      case 64: return active_clusters_t<64, true, true>(p);
+      default: return 0;
+    }
+  }
 #define MXFP4_OCC(BM_) \
-  case BM_: return fused ? active_clusters_t<BM_, true>(p) : active_clusters_t<BM_, false>(p);
+  case BM_: return fused ? active_clusters_t<BM_, true, false>(p) : active_clusters_t<BM_, false, false>(p);
   switch (p.block_m) {
     MXFP4_OCC(16)
     MXFP4_OCC(32)
@@ -847,20 +995,24 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // split's K tiles).  Ties prefer the larger block_m (fewer re-reads of the
 // weights), then the larger stage count, then fewer splits.
 // Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
-// the estimate is not (keyed on the shape): sweeps of block_m x splits x stages, graph-replayed
-// calls with rotating operands.  `fused` is the GEMM kernel's kind (the large-M
-// shapes run the pre-quantized kernel on the fused entry's two-pass route).
+// the estimate is not (keyed on the shape): sweeps of block_m x splits x
+// stages x share, graph-replayed calls with rotating operands.  `fused` is the
+// GEMM kernel's kind (the large-M shapes run the pre-quantized kernel on the
+// fused entry's two-pass route).  Sharing the quantization along N measured
+// faster only at 16 x 3072 x 1536 (3.95 -> 3.77 us); at the K = 512 and
+// M >= 64 shapes the cluster start-up and the pushes cost more than the
+// quantization they save.
 struct TunedPlan {
   int64_t M, N, K;
   bool fused;
-  int block_m, splits, stages;
+  int block_m, splits, stages, share;
 };
 constexpr TunedPlan kTunedPlans[] = {
-    {16, 2112, 7168, true, 16, 7, 4},
-    {8, 2112, 7168, true, 16, 7, 4},
-    {16, 3072, 1536, true, 16, 2, 3},
-    {64, 7168, 2048, false, 64, 2, 4},
-    {256, 3072, 1536, false, 64, 1, 6},
+    {16, 2112, 7168, true, 16, 7, 4, 1},
+    {8, 2112, 7168, true, 16, 7, 4, 1},
+    {16, 3072, 1536, true, 16, 3, 2, 2},
+    {64, 7168, 2048, false, 64, 2, 4, 1},
+    {256, 3072, 1536, false, 64, 1, 6, 1},
 };
 
 // Estimated critical path of one CTA, in ns (see above).
@@ -881,6 +1033,7 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
     q.block_m = t.block_m;
     q.splits = t.splits;
     q.stages = t.stages;
+    q.share = t.share;
     if (!finish_plan(M, N, K, fused, prop, &q)) continue;
     const int64_t ctas = static_cast<int64_t>(q.grid_y) * q.grid_z * q.splits;
     if (ctas <= 2 * static_cast<int64_t>(prop.multiProcessorCount)) {

@@ -70,6 +70,7 @@ struct GemmArgs {
   int32_t c_tma;            // no K split: C leaves through a bf16 tile in shared memory and one TMA store
   int32_t trigger_late;     // let the next grid launch only once this grid has passed its own wait
   int32_t abf_ring;         // fused: bf16 staging buffers (a ring of its own, at most kAbfRing)
+  int32_t share;            // CTAs along N sharing the quantization of their rows (1: none)
 };
 
 // bf16 activation buffers of the fused kernel: tile i is staged in buffer

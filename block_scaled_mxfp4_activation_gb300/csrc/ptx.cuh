@@ -374,6 +374,35 @@ __device__ __forceinline__ void cluster_sync_all() {
                    : "memory");
 }
 
+// This CTA's coordinates inside its thread-block cluster.
+__device__ __forceinline__ uint32_t cluster_ctaid_x() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctaid.x;" : "=r"(r));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_ctaid_y() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctaid.y;" : "=r"(r));
+  return r;
+}
+
+// Asynchronous stores into a cluster CTA's shared memory (shared::cluster
+// addresses, from map_to_rank) that count their bytes on that CTA's mbarrier
+// `cbar` (complete_tx): the receiver waits on its own barrier, armed with the
+// number of bytes it expects, and needs no other synchronisation.
+__device__ __forceinline__ void st_async_v2(uint32_t caddr, uint32_t a, uint32_t b, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(caddr),
+               "r"(a), "r"(b), "r"(cbar)
+               : "memory");
+}
+
+__device__ __forceinline__ void st_async_b32(uint32_t caddr, uint32_t a, uint32_t cbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr), "r"(a),
+               "r"(cbar)
+               : "memory");
+}
+
 // Address of the same shared-memory offset in cluster CTA `rank`.
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   uint32_t r;

@@ -70,6 +70,10 @@ typedef struct {
                          codes (this plan then describes that GEMM) */
   int32_t accumulators; /* independent fp32 accumulator tiles in tensor memory: 1, 2 or 4
                            (K step g goes to tile g mod accumulators; summed in the epilogue) */
+  int32_t share;      /* fused entry: CTAs of neighbouring N tiles that quantize the activation once
+                         between them (each a share of the K tiles, pushed into the others' shared
+                         memory); 1 = each CTA quantizes its own, 0 = the default choice.  The
+                         cluster is splits x share CTAs */
 } mxfp4_plan_t;
 
 /* ---------------------------------------------------------------------------
@@ -278,8 +282,9 @@ mxfp4_status_t mxfp4_chain_plan(int64_t M, int64_t K, int32_t num_layers, const 
  * fused entry.  Host only, launches nothing. */
 mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4_plan_t* plan);
 
-/* The GEMM entries with an explicit plan: only block_m, splits, stages and
- * accumulators (0 = the default choice) are read (the rest is derived); a plan
+/* The GEMM entries with an explicit plan: only block_m, splits, stages,
+ * accumulators and share (0 = the default choice) are read (the rest is
+ * derived; a plan with share > 1 takes a stage per K tile); a plan
  * the device cannot run is rejected with
  * MXFP4_ERR_INVALID_ARG.  fused != 0 reads A/lda, else Aq/As. */
 mxfp4_status_t mxfp4_gemm_with_plan(const void* A_or_Aq, int64_t lda, const void* As,

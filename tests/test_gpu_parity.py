@@ -200,6 +200,68 @@ def test_fused_quantization_bitexact_through_identity(oracle_mod, M):
         assert not bad.any(), f"{what}: {int(bad.sum())} of {bad.size} differ, first at {np.argwhere(bad)[0]}"
 
 
+@pytest.mark.parametrize("M", [37, 64])
+def test_shared_quantization_bitexact_through_identity(oracle_mod, M):
+    """Plans whose CTAs along N quantize the activation once between them (each a
+    share of the K tiles, pushed into the others' shared memory): through B = I
+    every output is one dequantized activation element, so the shared
+    quantization is checked bit for bit (ties, signed zeros, tiny values,
+    all-zero blocks), for every share count, block_m and K split that applies."""
+    K = 1024  # 8 N tiles of the identity, 4 K tiles
+    A = grid_activation(M, K, seed=M + 11)
+    B = torch.eye(K, dtype=torch.float32).to(torch.bfloat16)
+    _, _, W = quantized_weight(oracle_mod, B)
+    aq, as_ = oracle_mod.quantize(A)
+    expect = oracle_mod.dequantize(aq, as_)
+    Ad = A.cuda()
+    ran = 0
+    for bm in (16, 32, 64):
+        for splits, share in ((1, 2), (1, 4), (2, 2), (1, 8), (2, 4)):
+            plan = {"block_m": bm, "splits": splits, "share": share}
+            try:
+                C = mx.gemm_with_plan(Ad, None, W, plan, True)
+            except mx.MXFP4Error as e:
+                assert e.status == 1, plan  # does not fit (shared memory) or share > K tiles per split
+                continue
+            got = C.float().cpu().numpy().astype(np.float64)
+            bad = got != expect
+            assert not bad.any(), f"{plan}: {int(bad.sum())} of {bad.size} differ, first at {np.argwhere(bad)[0]}"
+            ran += 1
+    assert ran == 9  # share <= K tiles per split: (1, 2), (1, 4), (2, 2) at each block_m
+    assert mx.device_error(reset=True) == 0
+
+
+@pytest.mark.parametrize("M,N,K", [(40, 384, 1568), (5, 512, 1024), (64, 1024, 2048), (100, 256, 1536), (16, 768, 7168)])
+def test_shared_quantization_plans_against_oracle(oracle_mod, M, N, K):
+    """Shared quantization on ragged shapes (M tails, a K tail, 3-way shares)
+    against the oracle, and equal to the plain fused kernel's result where the
+    K split is the same (identical codes, identical sums)."""
+    A, B = workloads.make_random(M, N, K, seed=M + N + K)
+    bq, bs, W = quantized_weight(oracle_mod, B)
+    _, _, c64, _ = oracle_mod.quant_gemm(A, bq, bs)
+    Ad = A.cuda()
+    n_tiles = -(-N // 128)
+    ran = 0
+    for bm in (16, 32, 64):
+        for splits in (1, 2, 4):
+            for share in (2, 3, 4):
+                if n_tiles % share:
+                    continue
+                plan = {"block_m": bm, "splits": splits, "share": share}
+                try:
+                    C = mx.gemm_with_plan(Ad, None, W, plan, True)
+                except mx.MXFP4Error as e:
+                    assert e.status == 1, plan
+                    continue
+                check_close(C, c64, f"plan {plan} {M}x{N}x{K}")
+                ref = mx.gemm_with_plan(Ad, None, W, {"block_m": bm, "splits": splits, "share": 1,
+                                                      "stages": -(-(-(-K // 256)) // splits)}, True)
+                assert torch.equal(C, ref), f"plan {plan}: differs from the unshared kernel"
+                ran += 1
+    assert ran >= 3
+    assert mx.device_error(reset=True) == 0
+
+
 def random_shapes(n: int, seed: int):
     """Seeded (M, N, K) with tails in every dimension: M 1..96, N 1..400,
     K a multiple of 32 up to 1536 (K % 256 and K % 64 both vary)."""
