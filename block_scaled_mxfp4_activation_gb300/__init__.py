@@ -11,6 +11,7 @@ raised.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -69,41 +70,64 @@ def load_library(build_if_missing: bool = True) -> ctypes.CDLL:
         if _lib is not None:
             return _lib
         path = _build.build() if build_if_missing else _build.LIB
-        if not os.path.exists(path):
-            raise RuntimeError(f"libmxfp4.so not found at {path}; run build() first")
-        lib = ctypes.CDLL(path)
-        P, I, S, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
-        st = ctypes.c_int
-        sig = {
-            "mxfp4_quantize": ([P, I, I, I, P, P, S], st),
-            "mxfp4_packed_weight_bytes": ([I, I], Z),
-            "mxfp4_pack_weights": ([P, P, I, I, P, S], st),
-            "mxfp4_unpack_weights": ([P, I, I, P, P, S], st),
-            "mxfp4_pack_weights_shuffled": ([P, P, I, I, P, S], st),
-            "mxfp4_workspace_bytes": ([I, I, I], Z),
-            "mxfp4_gemm": ([P, P, P, P, I, I, I, P, Z, S], st),
-            "mxfp4_quant_gemm": ([P, I, P, P, I, I, I, P, Z, S], st),
-            "mxfp4_gemm_plan": ([I, I, I, ctypes.c_int, ctypes.POINTER(Plan)], st),
-            "mxfp4_gemm_with_plan": ([P, I, P, P, P, I, I, I, ctypes.c_int, ctypes.POINTER(Plan), S], st),
-            "mxfp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
-            "mxfp4_device_error": ([S, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], st),
-            "mxfp4_set_wait_timeout_ns": ([ctypes.c_uint64], st),
-            "mxfp4_diag_wait_timeout": ([S], st),
-            "mxfp4_set_programmatic_launch": ([ctypes.c_int], st),
-            "mxfp4_last_error_string": ([], ctypes.c_char_p),
-            "mxfp4_quant_gemm_host": ([P, I, P, I, P, P, P, I, I, I, P, Z, S], st),
-            "mxfp4_chain_workspace_bytes": ([I, I, ctypes.c_int32, ctypes.POINTER(I)], Z),
-            "mxfp4_quant_gemm_chain": ([P, I, I, I, ctypes.c_int32, ctypes.POINTER(P), ctypes.POINTER(I),
-                                        ctypes.POINTER(P), P, Z, S], st),
-            "mxfp4_chain_plan": ([I, I, ctypes.c_int32, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_int32),
-                                  ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], st),
-        }
-        for name, (args, res) in sig.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = res
-        _lib = lib
-        return lib
+        _lib = _open(path)
+        return _lib
+
+
+@contextlib.contextmanager
+def checked_library():
+    """Within the block every call of this module goes to libmxfp4_checked.so,
+    the build whose kernels test each computed index against its buffer and
+    report a miss in the device error word (bit 8) instead of making the
+    access.  It is compiled on first use; its device state (error word, wait
+    timeout, launch mode) is its own."""
+    global _lib
+    normal = load_library()
+    with _lock:
+        checked = _open(_build.build(checked=True))
+        _lib = checked
+    try:
+        yield checked
+    finally:
+        with _lock:
+            _lib = normal
+
+
+def _open(path: str) -> ctypes.CDLL:
+    if not os.path.exists(path):
+        raise RuntimeError(f"{os.path.basename(path)} not found at {path}; run build() first")
+    lib = ctypes.CDLL(path)
+    P, I, S, Z = ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t
+    st = ctypes.c_int
+    sig = {
+        "mxfp4_quantize": ([P, I, I, I, P, P, S], st),
+        "mxfp4_packed_weight_bytes": ([I, I], Z),
+        "mxfp4_pack_weights": ([P, P, I, I, P, S], st),
+        "mxfp4_unpack_weights": ([P, I, I, P, P, S], st),
+        "mxfp4_pack_weights_shuffled": ([P, P, I, I, P, S], st),
+        "mxfp4_workspace_bytes": ([I, I, I], Z),
+        "mxfp4_gemm": ([P, P, P, P, I, I, I, P, Z, S], st),
+        "mxfp4_quant_gemm": ([P, I, P, P, I, I, I, P, Z, S], st),
+        "mxfp4_gemm_plan": ([I, I, I, ctypes.c_int, ctypes.POINTER(Plan)], st),
+        "mxfp4_gemm_with_plan": ([P, I, P, P, P, I, I, I, ctypes.c_int, ctypes.POINTER(Plan), S], st),
+        "mxfp4_status_string": ([ctypes.c_int], ctypes.c_char_p),
+        "mxfp4_device_error": ([S, ctypes.c_int, ctypes.POINTER(ctypes.c_uint32)], st),
+        "mxfp4_set_wait_timeout_ns": ([ctypes.c_uint64], st),
+        "mxfp4_diag_wait_timeout": ([S], st),
+        "mxfp4_set_programmatic_launch": ([ctypes.c_int], st),
+        "mxfp4_last_error_string": ([], ctypes.c_char_p),
+        "mxfp4_quant_gemm_host": ([P, I, P, I, P, P, P, I, I, I, P, Z, S], st),
+        "mxfp4_chain_workspace_bytes": ([I, I, ctypes.c_int32, ctypes.POINTER(I)], Z),
+        "mxfp4_quant_gemm_chain": ([P, I, I, I, ctypes.c_int32, ctypes.POINTER(P), ctypes.POINTER(I),
+                                    ctypes.POINTER(P), P, Z, S], st),
+        "mxfp4_chain_plan": ([I, I, ctypes.c_int32, ctypes.POINTER(I), ctypes.POINTER(ctypes.c_int32),
+                              ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int32)], st),
+    }
+    for name, (args, res) in sig.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
+    return lib
 
 
 def status_string(status: int) -> str:

@@ -264,6 +264,7 @@ mxfp4_status_t prepare_gemm(const void* a, int64_t lda, const void* as, const vo
   g.abf_off = GL.abf_off;
   g.abf_stage_bytes = GL.abf_stage;
   g.abf_ring = GL.abf_ring;
+  g.smem_total = GL.total;
   g.share = fused ? plan.share : 1;
   g.sfw_off = GL.sfw_off;
   g.sfa_off = GL.sfa_off;

@@ -287,7 +287,11 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
         const int r_t = 16 * g + (tid >> 4), j = tid & 15;
         const int m = m_tile * BM + r_t;
         const int col = kt * kTileK + j * 16;
-        const bool valid = m < M && col < p.K0;
+        const bool valid = m < M && col < p.K0 &&
+                           MXFP4_IN_BOUNDS(static_cast<int64_t>(m) * p.lda + col + 16 <= static_cast<int64_t>(M) * p.lda &&
+                                               static_cast<int64_t>(m) * (p.K0 / 2) + col / 2 + 8 <=
+                                                   static_cast<int64_t>(M) * (p.K0 / 2),
+                                           p.err);
         uint4 v = make_uint4(0, 0, 0, 0), w = make_uint4(0, 0, 0, 0);
         if (valid) {
           const uint16_t* src = p.a + static_cast<int64_t>(m) * p.lda + col;
@@ -360,7 +364,9 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
               v = src[0];
               w = src[1];
               uint16_t* crow = reinterpret_cast<uint16_t*>(L.c) + static_cast<int64_t>(m_base + m) * N;
-              if (vec && n0 + 16 <= N) {
+              // (no early exit: every lane reaches the pair shuffle below)
+              if (!MXFP4_IN_BOUNDS(m_base + m < M, p.err)) {
+              } else if (vec && n0 + 16 <= N) {
                 *reinterpret_cast<uint4*>(crow + n0) = v;
                 *reinterpret_cast<uint4*>(crow + n0 + 8) = w;
               } else if (vec && n0 + 8 <= N) {
@@ -376,7 +382,10 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
             const uint32_t byte = scale_byte_from_amax(amax);
             const uint16_t sbf = scale_bf16_from_byte(byte);
             const uint32_t c0 = e2m1_pack8(v, sbf), c1 = e2m1_pack8(w, sbf);
-            if (valid && n_base + 16 * j < N)
+            if (valid && n_base + 16 * j < N &&
+                MXFP4_IN_BOUNDS(static_cast<int64_t>(m_base + m) * (N / 2) + n_base / 2 + 8 * j + 8 <=
+                                    static_cast<int64_t>(M) * (N / 2),
+                                p.err))
               *reinterpret_cast<uint2*>(L.out_codes + static_cast<int64_t>(m_base + m) * (N / 2) + n_base / 2 + 8 * j) =
                   make_uint2(c0, c1);
             if (valid && (j & 1) == 0)
@@ -425,6 +434,7 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
             tmem_ld_32x32b_x16(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + c * 16, r);
             tmem_ld_wait();
             float* dst = part + (static_cast<size_t>(it.split) * BM + 16 * c) * kTileN + 32 * q + lane;
+            if (!MXFP4_IN_BOUNDS(tile < L.n_tiles * p.m_tiles && it.split < S, p.err)) break;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
               if (16 * c + e < m_valid) dst[e * kTileN] = __uint_as_float(r[e]);

@@ -213,6 +213,13 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   // K steps (of 64) in this split's last K tile
   const int steps_last = kt_count > 0 ? min(4, (args.K - (kt_end - 1) * kTileK + 63) / 64) : 0;
   const uint64_t timeout = args.timeout_ns;
+  // checked build: flat element index into C, byte range in this CTA's shared memory
+  auto c_ok = [&](int64_t idx, int64_t width) {
+    return MXFP4_IN_BOUNDS(idx >= 0 && idx + width <= static_cast<int64_t>(args.M) * args.N, args.err);
+  };
+  auto smem_ok = [&](uint32_t off, uint32_t bytes) { return MXFP4_IN_BOUNDS(off + bytes <= args.smem_total, args.err); };
+  (void)c_ok;
+  (void)smem_ok;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
@@ -471,6 +478,11 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     auto load_scales = [&](int i, uint32_t& w0, uint32_t& w1) {
       const int64_t j0 = static_cast<int64_t>(kt_begin + i) * 8;
       const uint8_t* src = args.a_scales + static_cast<int64_t>(m_base + tid) * nblk + j0;
+      if (!MXFP4_IN_BOUNDS(static_cast<int64_t>(m_base + tid) * nblk + j0 < static_cast<int64_t>(args.M) * nblk,
+                           args.err)) {
+        w0 = w1 = 0u;
+        return;
+      }
       if (scales_vec8) {
         const uint2 v = ld_after_wait_v2(src);  // written by the quantize pass before this grid
         w0 = v.x;
@@ -640,12 +652,14 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
           __nv_bfloat16* col = args.c + static_cast<int64_t>(m_base) * args.N + n;
 #pragma unroll
           for (int e = 0; e < 16; ++e)
-            if (c * 16 + e < m_valid) col[static_cast<int64_t>(c * 16 + e) * args.N] = __float2bfloat16_rn(__uint_as_float(r[e]));
+            if (c * 16 + e < m_valid && c_ok((static_cast<int64_t>(m_base) + c * 16 + e) * args.N + n, 1))
+              col[static_cast<int64_t>(c * 16 + e) * args.N] = __float2bfloat16_rn(__uint_as_float(r[e]));
           if constexpr (kHostC) {
             __nv_bfloat16* hcol = args.c_host + static_cast<int64_t>(m_base) * args.N + n;
 #pragma unroll
             for (int e = 0; e < 16; ++e)
-              if (c * 16 + e < m_valid) hcol[static_cast<int64_t>(c * 16 + e) * args.N] = __float2bfloat16_rn(__uint_as_float(r[e]));
+              if (c * 16 + e < m_valid && c_ok((static_cast<int64_t>(m_base) + c * 16 + e) * args.N + n, 1))
+                hcol[static_cast<int64_t>(c * 16 + e) * args.N] = __float2bfloat16_rn(__uint_as_float(r[e]));
           }
         }
         continue;
@@ -661,11 +675,12 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       if (owner == rank) {  // this CTA's own blocks: plain shared-memory stores
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          *reinterpret_cast<float*>(smem + (dst - sbase) + e * 128) = __uint_as_float(r[e]);
+          if (smem_ok(dst - sbase + e * 128, 4)) *reinterpret_cast<float*>(smem + (dst - sbase) + e * 128) = __uint_as_float(r[e]);
       } else {
         const uint32_t cdst = map_to_rank(dst, owner + static_cast<uint32_t>(splits) * share_rank);
 #pragma unroll
-        for (int e = 0; e < 16; ++e) st_cluster_f32(cdst + e * 128, __uint_as_float(r[e]));
+        for (int e = 0; e < 16; ++e)
+          if (smem_ok(dst - sbase + e * 128, 4)) st_cluster_f32(cdst + e * 128, __uint_as_float(r[e]));
       }
     }
     if (splits == 1 && c_tma) {
@@ -682,7 +697,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         const int n_base = n_tile * kTileN;
         for (int it = tid; it < m_valid * 16; it += C::kAThreads) {
           const int m = it >> 4, n = n_base + (it & 15) * 8;
-          if (n < args.N)
+          if (n < args.N && c_ok(static_cast<int64_t>(m_base + m) * args.N + n, 8))
             *reinterpret_cast<uint4*>(args.c_host + static_cast<int64_t>(m_base + m) * args.N + n) =
                 *reinterpret_cast<const uint4*>(smem + (m * kTileN + (it & 15) * 8) * 2);
         }
@@ -719,6 +734,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       const int m = (bi >> 2) * 16 + row;
       if (m >= m_valid) continue;
       const uint32_t off = lb * kBlockBytes + row * 128 + c4 * 16;
+      if (!smem_ok(args.stg_off + (splits - 1) * stg_stride + off, 16)) continue;
       float4 acc = ld_shared_f4(stg + off);
       for (int src = 1; src < splits; ++src) {
         const float4 p = ld_shared_f4(stg + src * stg_stride + off);
@@ -727,6 +743,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       const int64_t gm = static_cast<int64_t>(m_base) + m;
       const int gn = n_base + (bi & 3) * 32 + c4 * 4;
       __nv_bfloat16* dst = c_out + gm * n_cols + gn;
+      // columns past N are never stored: only the stored ones are checked
+      if (!(gn >= n_cols || c_ok(gm * n_cols + gn, min(4, n_cols - gn)))) continue;
       if (vec_ok && gn + 3 < n_cols) {
         const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
         const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);

@@ -18,7 +18,8 @@ namespace mxfp4 {
 // after the wait (the destination may still be read by the previous kernel).
 __global__ void __launch_bounds__(256) copy_rows_kernel(const uint8_t* __restrict__ src, int64_t src_pitch,
                                                         uint8_t* __restrict__ dst, int64_t dst_pitch,
-                                                        int64_t row_bytes, int64_t rows, int src_early) {
+                                                        int64_t row_bytes, int64_t rows, int src_early,
+                                                        uint32_t* err) {
   grid_launch_dependents();
   const int64_t per_row = row_bytes / 16;
   const int64_t total = per_row * rows;
@@ -27,15 +28,18 @@ __global__ void __launch_bounds__(256) copy_rows_kernel(const uint8_t* __restric
   if (src_early && i < total && i + stride >= total) {
     // one element per thread: load, then wait, then store
     const int64_t r = i / per_row, c = i - r * per_row;
-    const uint4 v = *reinterpret_cast<const uint4*>(src + r * src_pitch + c * 16);
+    const bool ok = MXFP4_IN_BOUNDS(r < rows && c * 16 + 16 <= row_bytes, err);
+    uint4 v = make_uint4(0, 0, 0, 0);
+    if (ok) v = *reinterpret_cast<const uint4*>(src + r * src_pitch + c * 16);
     grid_dependency_wait();
-    *reinterpret_cast<uint4*>(dst + r * dst_pitch + c * 16) = v;
+    if (ok) *reinterpret_cast<uint4*>(dst + r * dst_pitch + c * 16) = v;
     return;
   }
   grid_dependency_wait();
   for (; i < total; i += stride) {  // the source may be the previous grid's output
     const int64_t r = i / per_row, c = i - r * per_row;
-    *reinterpret_cast<uint4*>(dst + r * dst_pitch + c * 16) = ld_after_wait_v4(src + r * src_pitch + c * 16);
+    if (MXFP4_IN_BOUNDS(r < rows && c * 16 + 16 <= row_bytes, err))
+      *reinterpret_cast<uint4*>(dst + r * dst_pitch + c * 16) = ld_after_wait_v4(src + r * src_pitch + c * 16);
   }
 }
 
@@ -57,7 +61,8 @@ cudaError_t launch_copy_rows(const void* src, int64_t src_pitch, void* dst, int6
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, copy_rows_kernel, static_cast<const uint8_t*>(src), src_pitch,
-                            static_cast<uint8_t*>(dst), dst_pitch, row_bytes, rows, src_early ? 1 : 0);
+                            static_cast<uint8_t*>(dst), dst_pitch, row_bytes, rows, src_early ? 1 : 0,
+                            device_error_word());
 }
 
 }  // namespace mxfp4

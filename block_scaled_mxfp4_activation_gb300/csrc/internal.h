@@ -71,6 +71,7 @@ struct GemmArgs {
   int32_t trigger_late;     // let the next grid launch only once this grid has passed its own wait
   int32_t abf_ring;         // fused: bf16 staging buffers (a ring of its own, at most kAbfRing)
   int32_t share;            // CTAs along N sharing the quantization of their rows (1: none)
+  uint32_t smem_total;      // bytes of the shared-memory layout (bounds of the checked build)
 };
 
 // bf16 activation buffers of the fused kernel: tile i is staged in buffer

@@ -20,11 +20,26 @@ enum DeviceError : uint32_t {
   kErrDiag = 1u << 5,        // the diagnostic kernel's wait (expected to give up)
   kErrBadPlan = 1u << 6,     // launch geometry disagrees with the kernel
   kErrWaitFlag = 1u << 7,    // a wait on another CTA's completion counter (multi-layer kernel)
+  kErrBounds = 1u << 8,      // checked build: an index outside its buffer (the access was skipped)
 };
 
 __device__ __forceinline__ void report_error(uint32_t* word, uint32_t bits) {
   if (word != nullptr) atomicOr(word, bits);
 }
+
+// Guard of a computed-index memory access.  In the library's checked build
+// (-DMXFP4_CHECKED) it tests the index against its buffer, and on failure
+// reports kErrBounds and returns false so the access is skipped; in the normal
+// build it is `true` and costs nothing.
+#ifdef MXFP4_CHECKED
+__device__ __forceinline__ bool in_bounds(bool ok, uint32_t* err) {
+  if (!ok) report_error(err, kErrBounds);
+  return ok;
+}
+#define MXFP4_IN_BOUNDS(cond, err) ::mxfp4::in_bounds((cond), (err))
+#else
+#define MXFP4_IN_BOUNDS(cond, err) true
+#endif
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

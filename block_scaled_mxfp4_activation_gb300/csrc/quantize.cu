@@ -32,7 +32,7 @@ uint32_t* device_error_word() {
 __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restrict__ A, int64_t M,
                                                        int64_t K, int64_t lda,
                                                        uint8_t* __restrict__ Aq,
-                                                       uint8_t* __restrict__ As) {
+                                                       uint8_t* __restrict__ As, uint32_t* err) {
   const int64_t units_per_row = K / 16;
   const int64_t unit = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
   const bool valid = unit < M * units_per_row;
@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   if (valid && (j & 3) == 0) asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
   grid_dependency_wait();
   uint4 v = make_uint4(0, 0, 0, 0), w = make_uint4(0, 0, 0, 0);
-  if (valid) {
+  if (valid && MXFP4_IN_BOUNDS(row * lda + j * 16 + 16 <= M * lda, err)) {
     v = ld_after_wait_v4(src);  // A may be the previous grid's output
     w = ld_after_wait_v4(src + 8);
   }
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(256) quantize_kernel(const uint16_t* __restric
   const uint32_t byte = scale_byte_from_amax(amax);
   const uint16_t sbf = scale_bf16_from_byte(byte);
   const uint32_t c0 = e2m1_pack8(v, sbf), c1 = e2m1_pack8(w, sbf);
-  if (valid) {
+  if (valid && MXFP4_IN_BOUNDS(row * (K / 2) + j * 8 + 8 <= M * (K / 2), err)) {
     *reinterpret_cast<uint2*>(Aq + row * (K / 2) + j * 8) = make_uint2(c0, c1);
     if ((j & 1) == 0) As[row * (K / 32) + j / 2] = static_cast<uint8_t>(byte);
   }
@@ -76,7 +76,7 @@ cudaError_t launch_quantize(const void* A, int64_t M, int64_t K, int64_t lda, vo
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, quantize_kernel, static_cast<const uint16_t*>(A), M, K, lda,
-                            static_cast<uint8_t*>(Aq), static_cast<uint8_t*>(As));
+                            static_cast<uint8_t*>(Aq), static_cast<uint8_t*>(As), device_error_word());
 }
 
 // ----------------------------------------------------------------------------- weight relayout
