@@ -109,6 +109,65 @@ __device__ __forceinline__ void quantize_tile(const uint8_t* abf, uint8_t* a_til
   }
 }
 
+// Direct activation path of the fused kernel (block_m 16 or 32, no shared
+// quantization): each producer thread loads its units of a group of up to
+// 4 / (BM / 16) K tiles straight from global memory -- every load of the group
+// in flight at once, no staging buffer and no per-tile barrier -- then
+// quantizes them into the group's stages.  The unit layout is quantize_tile's
+// (unit u = tid + kThreads * e: row u / 16, 16 elements (u % 16) * 16 of the
+// K tile); units past K read as zeros (as a zero-filled TMA box would), rows
+// past m_valid are neither loaded nor stored.
+template <int BM, int kThreads>
+struct DirectTiles {
+  static constexpr int kUnits = BM * 16 / kThreads;  // units per thread and K tile
+  static constexpr int kGroup = 4 / kUnits;          // K tiles per group
+  uint4 v[kGroup][kUnits][2];
+
+  __device__ __forceinline__ void load(const uint8_t* a, int64_t lda_bytes, int m_base, int m_valid, int K,
+                                       int kt0, int n, int tid, int M, uint32_t* err) {
+    (void)M;
+    (void)err;
+#pragma unroll
+    for (int j = 0; j < kGroup; ++j)
+#pragma unroll
+      for (int e = 0; e < kUnits; ++e) {
+        const int u = tid + e * kThreads, m = u >> 4;
+        const int col = (kt0 + j) * kTileK + (u & 15) * 16;
+        v[j][e][0] = v[j][e][1] = make_uint4(0u, 0u, 0u, 0u);
+        if (j < n && m < m_valid && col < K &&
+            MXFP4_IN_BOUNDS(static_cast<int64_t>(m_base + m) * lda_bytes + static_cast<int64_t>(col) * 2 + 32 <=
+                                static_cast<int64_t>(M) * lda_bytes,
+                            err)) {
+          const uint8_t* src = a + static_cast<int64_t>(m_base + m) * lda_bytes + static_cast<int64_t>(col) * 2;
+          v[j][e][0] = ld_after_wait_v4(src);  // A may be the previous grid's output
+          v[j][e][1] = ld_after_wait_v4(src + 16);
+        }
+      }
+  }
+
+  // Quantizes tile j of the group into a_tile / sfa (one stage).  The pair
+  // shuffle needs both lanes of a block: a warp's units are skipped only when
+  // both of its rows are past m_valid (warp-uniform).
+  __device__ __forceinline__ void quantize(int j, uint8_t* a_tile, uint8_t* sfa, int tid, int m_valid) const {
+    const int pw = tid >> 5, half = tid & 1;
+#pragma unroll
+    for (int e = 0; e < kUnits; ++e) {
+      if (2 * pw + 16 * e >= m_valid) continue;  // warp-uniform
+      const int u = tid + e * kThreads;
+      const int m = u >> 4, b = (u >> 1) & 7;
+      uint32_t amax = absmax16_bf16(v[j][e][0], v[j][e][1]);
+      amax = max(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      const uint32_t byte = scale_byte_from_amax(amax);
+      const uint16_t sbf = scale_bf16_from_byte(byte);
+      const uint32_t w0 = e2m1_pack8(v[j][e][0], sbf), w1 = e2m1_pack8(v[j][e][1], sbf);
+      if (m < m_valid) {
+        *reinterpret_cast<uint2*>(a_tile + m * kTileKBytes + ((b ^ (m & 7)) << 4) + 8 * half) = make_uint2(w0, w1);
+        if (half == 0) sfa[(b >> 2) * kSfChunkBytes + sf_chunk_offset(m) + (b & 3)] = static_cast<uint8_t>(byte);
+      }
+    }
+  }
+};
+
 // The same quantization for a tile shared along N: the tile's codes and the
 // scale words of its rows go to the same stage of every CTA that shares it
 // (`share` CTAs, cluster ranks rank0 + rank_step * t), by st.async completing
@@ -180,6 +239,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     mxfp4_gemm_kernel(const __grid_constant__ CUtensorMap tmap_b, const __grid_constant__ CUtensorMap tmap_a,
                       const __grid_constant__ CUtensorMap tmap_c, const GemmArgs args) {
   using C = TileCfg<BM, kFused>;
+  // fused, block_m <= 32, not shared: activation straight from global memory
+  // into registers (DirectTiles); otherwise by TMA into shared memory
+  constexpr bool kDirect = kFused && !kShare && BM <= 32;
   extern __shared__ __align__(1024) uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const uint32_t sbase = smem_u32(smem);
@@ -333,14 +395,15 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       for (int i = 0; i < pre; ++i) issue_w(i, i);
     const int ring_a = kFused ? args.abf_ring : stages;  // activation buffers
     // kShare: this CTA loads (and quantizes) only K tiles share_rank, + share, ...
-    const int own = kShare ? (kt_count - static_cast<int>(share_rank) + share - 1) / share : kt_count;
+    const int own = kDirect ? 0 : kShare ? (kt_count - static_cast<int>(share_rank) + share - 1) / share : kt_count;
     const int pre_a = min(ring_a, own);
     if constexpr (kShare) {
       for (int j = 0; j < pre_a; ++j) issue_a(static_cast<int>(share_rank) + j * share, j);
     } else {
       for (int i = 0; i < pre_a; ++i) issue_a(i, i);
     }
-    if (args.trigger_late) grid_launch_dependents();
+    // (direct path: the producers trigger, once their loads have landed)
+    if (args.trigger_late && !kDirect) grid_launch_dependents();
     int issued_w = pre, issued_a = pre_a;
     // refills: a stage's weights once its MMAs are done; an activation buffer
     // once its tile is quantized (fused) or with its stage (unfused).  The
@@ -359,7 +422,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         issue_w(i, s);
         issued_w = i + 1;
       }
-      if (i < pre_a) continue;
+      if (kDirect || i < pre_a) continue;
       if constexpr (kFused) {
         const int r = i % ring_a, round_a = i / ring_a;
         ok = __all_sync(0xFFFFFFFFu, mbar_wait(abf_free(r), (round_a - 1) & 1, timeout));
@@ -386,57 +449,54 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     __syncwarp();
   } else if (warp == 1) {
     // ------------------------------------------------------------------ MMA issuer
-    // Warp-wide loop (uniform operands), one elected lane issues the tcgen05
-    // instructions; the same lane issues every commit, which tracks that
-    // lane's earlier operations.
-    const bool leader = elect_one();
-    bool triggered = !args.trigger_late;
-    // Weight scales of stage s to tensor memory once the stage's weights have
-    // landed; false if the wait gave up.
-    auto weight_scales = [&](int s, int round) {
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_w(s), round & 1, timeout))) {
-        if (leader) report_error(args.err, kErrWaitTma);
-        *abort_flag = 1u;
-      }
-      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) return false;
-      tc_fence_after_sync();
-      const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
-      const uint32_t sfw_s = sbase + args.sfw_off + s * kSfTileBytes;
-      if (leader) {
+    // One elected lane runs the whole role: it waits on the barriers, issues
+    // the tcgen05 copies and MMAs, and issues every commit (a commit tracks
+    // the issuing thread's earlier operations).  No warp votes or warp
+    // barriers on the per-tile path; the other lanes wait at the end.
+    if (elect_one()) {
+      bool triggered = !args.trigger_late;
+      // Weight scales of stage s to tensor memory once the stage's weights
+      // have landed; false if the wait gave up.
+      auto weight_scales = [&](int s, int round) {
+        if (!mbar_wait(full_w(s), round & 1, timeout)) {
+          report_error(args.err, kErrWaitTma);
+          *abort_flag = 1u;
+        }
+        if (*abort_flag != 0u) return false;
+        tc_fence_after_sync();
+        const uint32_t sfw_t = tmem_sf + s * C::kSfCols;  // weight scales: 2 chunks x 4 columns
+        const uint32_t sfw_s = sbase + args.sfw_off + s * kSfTileBytes;
 #pragma unroll
         for (int c = 0; c < 2; ++c) tmem_cp_32x128b_warpx4(sfw_t + 4 * c, smem_desc(sfw_s + c * kSfChunkBytes, 128, 128, 0));
-      }
-      __syncwarp();
-      return true;
-    };
-    // The stages loaded first hold weights that arrive before the activation
-    // (under programmatic launch, before the previous grid has finished): their
-    // scales go to tensor memory up front, off the activation's critical path.
-    const int pre = min(stages, kt_count);
-    uint32_t mma_a_off = args.a_off, mma_sfa_off = args.sfa_off;
-    int mma_k = args.K;
-    asm volatile("" : "+r"(mma_a_off), "+r"(mma_sfa_off), "+r"(mma_k));  // parameters read before the waits
-    bool alive = true;
-    for (int i = 0; i < pre && alive; ++i) alive = weight_scales(i, 0);
-    for (int i = 0, s = 0, round = 0; i < kt_count && alive; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
-      const uint32_t sfw_t = tmem_sf + s * C::kSfCols;
-      const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
-      const uint32_t sfa_s = sbase + mma_sfa_off + s * C::kSfaStageBytes;
-      const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
-      const uint64_t b_desc = smem_desc(sbase + mma_a_off + s * C::kATileBytes, 16, 1024, 2);
-      const int k0 = (kt_begin + i) * kTileK;
-      if (i >= stages && !weight_scales(s, round)) break;  // a reloaded stage
-      if (!__all_sync(0xFFFFFFFFu, mbar_wait(full_a(s), round & 1, timeout))) {
-        if (leader) report_error(args.err, kErrWaitA);
-        *abort_flag = 1u;
-      }
-      if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
-      if (!triggered) {  // the activation has landed: the next grid may start
-        grid_launch_dependents();
-        triggered = true;
-      }
-      tc_fence_after_sync();
-      if (leader) {
+        return true;
+      };
+      // The stages loaded first hold weights that arrive before the activation
+      // (under programmatic launch, before the previous grid has finished): their
+      // scales go to tensor memory up front, off the activation's critical path.
+      const int pre = min(stages, kt_count);
+      uint32_t mma_a_off = args.a_off, mma_sfa_off = args.sfa_off;
+      int mma_k = args.K;
+      asm volatile("" : "+r"(mma_a_off), "+r"(mma_sfa_off), "+r"(mma_k));  // parameters read before the waits
+      bool alive = true;
+      for (int i = 0; i < pre && alive; ++i) alive = weight_scales(i, 0);
+      for (int i = 0, s = 0, round = 0; i < kt_count && alive; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
+        const uint32_t sfw_t = tmem_sf + s * C::kSfCols;
+        const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
+        const uint32_t sfa_s = sbase + mma_sfa_off + s * C::kSfaStageBytes;
+        const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
+        const uint64_t b_desc = smem_desc(sbase + mma_a_off + s * C::kATileBytes, 16, 1024, 2);
+        const int k0 = (kt_begin + i) * kTileK;
+        if (i >= stages && !weight_scales(s, round)) break;  // a reloaded stage
+        if (!mbar_wait(full_a(s), round & 1, timeout)) {
+          report_error(args.err, kErrWaitA);
+          *abort_flag = 1u;
+        }
+        if (*abort_flag != 0u) break;
+        if (!triggered) {  // the activation has landed: the next grid may start
+          grid_launch_dependents();
+          triggered = true;
+        }
+        tc_fence_after_sync();
 #pragma unroll
         for (int c = 0; c < 2 * C::kRowChunks; ++c)
           tmem_cp_32x128b_warpx4(sfa_t + 4 * c, smem_desc(sfa_s + c * kSfChunkBytes, 128, 128, 0));
@@ -453,10 +513,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         }
         if (i + stages < kt_count) tc_commit(empty(s));  // frees the stage when these MMAs finish
       }
-      __syncwarp();
+      tc_commit(accum_bar);  // always: the epilogue waits on it
+      if (!triggered) grid_launch_dependents();
     }
-    if (leader) tc_commit(accum_bar);  // always: the epilogue waits on it
-    if (!triggered) grid_launch_dependents();
     __syncwarp();
   } else {
     // ------------------------------------------------------------------ activation producer
@@ -527,7 +586,42 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
             static_cast<uint32_t>(splits));
       }
     }
-    for (int i = 0, s = 0, round = 0, r = 0, round_a = 0; !kShare && i < kt_count;
+    if constexpr (kDirect) {
+      // groups of DirectTiles::kGroup K tiles (at most one per stage): the
+      // group's loads first, then, stage by stage, wait until the stage is
+      // free, quantize into it and hand it to the MMA warp
+      using D = DirectTiles<BM, C::kAThreads>;
+      const int group = min(D::kGroup, stages);
+      const uint8_t* a_glob = static_cast<const uint8_t*>(args.a);
+      int64_t lda_bytes = args.lda * 2;
+      int kdim = args.K;
+      asm volatile("" : "+l"(a_glob), "+l"(lda_bytes), "+r"(kdim));
+      D tiles;
+      for (int g0 = 0; g0 < kt_count; g0 += group) {
+        const int n = min(group, kt_count - g0);
+        tiles.load(a_glob, lda_bytes, m_base, m_valid, kdim, kt_begin + g0, n, tid, args.M, args.err);
+        if (!triggered) {  // this grid's activation loads are under way: the next grid may start
+          grid_launch_dependents();
+          triggered = true;
+        }
+#pragma unroll
+        for (int j = 0; j < D::kGroup; ++j) {
+          if (j >= n) break;
+          const int i = g0 + j, s = i % stages, round = i / stages;
+          if (round > 0 && !*abort_flag && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+            report_error(args.err, kErrWaitEmpty);
+            *abort_flag = 1u;
+          }
+          if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;  // warp-uniform: the shuffles need every lane
+          tiles.quantize(j, smem + a_off + s * C::kATileBytes, smem + sfa_off + s * C::kSfaStageBytes, tid, m_valid);
+          fence_proxy_async_smem();  // this thread's generic stores, visible to tcgen05
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_a(s));
+        }
+        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+      }
+    }
+    for (int i = 0, s = 0, round = 0, r = 0, round_a = 0; !kShare && !kDirect && i < kt_count;
          ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0, r = r + 1 < ring_a ? r + 1 : 0, round_a += r == 0) {
       if (round > 0 && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
         report_error(args.err, kErrWaitEmpty);
@@ -893,6 +987,7 @@ static bool plan_smem(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDe
 int abf_ring_for(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDeviceProp& prop) {
   if (!fused) return 0;
   if (p.share > 1) return (p.k_tiles_per_split + p.share - 1) / p.share;  // every own tile in flight
+  if (p.block_m <= 32) return 0;  // the direct path: activation loaded into registers
   // as many bf16 buffers as the split has K tiles (all in flight at once), up
   // to kAbfRing, as long as the CTA still fits -- and still shares an SM with
   // another CTA when it would with a single buffer
