@@ -479,19 +479,24 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       asm volatile("" : "+r"(mma_a_off), "+r"(mma_sfa_off), "+r"(mma_k));  // parameters read before the waits
       bool alive = true;
       for (int i = 0; i < pre && alive; ++i) alive = weight_scales(i, 0);
+      // stage 0's descriptors; stage s adds s tiles (the address field counts 16-byte units)
+      const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, 2);
+      const uint64_t b_desc0 = smem_desc(sbase + mma_a_off, 16, 1024, 2);
+      const uint32_t sfa_s0 = sbase + mma_sfa_off;
       for (int i = 0, s = 0, round = 0; i < kt_count && alive; ++i, s = s + 1 < stages ? s + 1 : 0, round += s == 0) {
         const uint32_t sfw_t = tmem_sf + s * C::kSfCols;
         const uint32_t sfa_t = sfw_t + 8;                 // activation scales: 2 x kRowChunks x 4
-        const uint32_t sfa_s = sbase + mma_sfa_off + s * C::kSfaStageBytes;
-        const uint64_t a_desc = smem_desc(sbase + s * C::kBTileBytes, 16, 1024, 2);
-        const uint64_t b_desc = smem_desc(sbase + mma_a_off + s * C::kATileBytes, 16, 1024, 2);
+        const uint32_t sfa_s = sfa_s0 + s * C::kSfaStageBytes;
+        const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(s * (C::kBTileBytes >> 4));
+        const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(s * (C::kATileBytes >> 4));
         const int k0 = (kt_begin + i) * kTileK;
         if (i >= stages && !weight_scales(s, round)) break;  // a reloaded stage
+        // (another role's abort shows up here as a wait that runs out)
         if (!mbar_wait(full_a(s), round & 1, timeout)) {
           report_error(args.err, kErrWaitA);
           *abort_flag = 1u;
+          break;
         }
-        if (*abort_flag != 0u) break;
         if (!triggered) {  // the activation has landed: the next grid may start
           grid_launch_dependents();
           triggered = true;
