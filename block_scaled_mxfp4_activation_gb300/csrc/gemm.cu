@@ -256,7 +256,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   auto full_in = [&](int r) { return sbase + args.bar_off + 8u * (3 * stages + r); }; // activation buffer (TMA)
   auto abf_free = [&](int r) { return sbase + args.bar_off + 8u * (3 * stages + nbuf + r); };
   const uint32_t accum_bar = sbase + args.bar_off + 8u * (3 * stages + 2 * nbuf);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + args.bar_off + 8 * (3 * stages + 2 * nbuf + 1));
+  // split-K: counts the bytes of the peers' partial blocks this CTA owns
+  const uint32_t red_bar = accum_bar + 8u;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + args.bar_off + 8 * (3 * stages + 2 * nbuf + 2));
   volatile uint32_t* abort_flag = tmem_slot + 1;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -305,6 +307,13 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       mbar_init(abf_free(r), C::kAWarps);
     }
     mbar_init(accum_bar, 1);
+    // split-K: armed with the bytes of the (splits - 1) peer partials of each
+    // block this CTA owns (blocks bi = rank, rank + splits, ... below valid_blocks)
+    if (splits > 1) {
+      mbar_init(red_bar, 1);
+      const int owned = (valid_blocks - static_cast<int>(rank) + splits - 1) / splits;
+      if (owned > 0) mbar_arrive_expect_tx(red_bar, static_cast<uint32_t>(owned * (splits - 1) * kBlockBytes));
+    }
     *abort_flag = 0u;
     fence_mbar_init();
   }
@@ -319,9 +328,15 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   }
   tc_fence_before_sync();
   __syncthreads();
-  // kShare: peers push into this CTA's buffers and barriers only after every
-  // CTA of the cluster has initialised its barriers
-  if constexpr (kShare) cluster_sync_all();
+  // Peers push into this CTA's buffers and barriers only after every CTA of
+  // the cluster has initialised its barriers: kShare waits here (its pushes
+  // start in the main loop); a K split arrives now and waits just before its
+  // epilogue pushes, by when every peer has long arrived.
+  if constexpr (kShare) {
+    cluster_sync_all();
+  } else {
+    if (splits > 1) cluster_arrive_release();
+  }
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
   const int nacc = args.accumulators;                 // independent accumulators (1, 2 or 4)
@@ -686,6 +701,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     if (!ok) report_error(args.err, kErrWaitAccum);
     tc_fence_after_sync();
     const bool have = ok && kt_count > 0 && !*abort_flag;
+    if (!kShare && splits > 1) cluster_wait_acquire();  // every peer's barriers are initialised
     const int qr = warp & 3;           // TMEM lanes this warp may read
     const int h = (warp - 2) >> 2;     // which half of the column chunks
     const int chunks = (m_valid + 15) >> 4;
@@ -765,8 +781,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       }
       // K split: block (chunk c of 16 activation rows, lane quarter qr) goes
       // to cluster rank (4c + qr) % splits, into that CTA's slot
-      // [this rank][(4c + qr) / splits].  The staging area is separate from
-      // the stage buffers, so a peer still running its MMAs is never disturbed.
+      // [this rank][(4c + qr) / splits], by st.async counted on the owner's
+      // red_bar (the owner waits for its bytes; no cluster barrier).  The
+      // staging area is separate from the stage buffers, so a peer still
+      // running its MMAs is never disturbed.
       const int bi = 4 * c + qr;
       const uint32_t owner = static_cast<uint32_t>(bi % splits);
       const uint32_t dst = sbase + args.stg_off +
@@ -776,10 +794,11 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         for (int e = 0; e < 16; ++e)
           if (smem_ok(dst - sbase + e * 128, 4)) *reinterpret_cast<float*>(smem + (dst - sbase) + e * 128) = __uint_as_float(r[e]);
       } else {
-        const uint32_t cdst = map_to_rank(dst, owner + static_cast<uint32_t>(splits) * share_rank);
+        const uint32_t peer = owner + static_cast<uint32_t>(splits) * share_rank;
+        const uint32_t cdst = map_to_rank(dst, peer), cbar = map_to_rank(red_bar, peer);
 #pragma unroll
         for (int e = 0; e < 16; ++e)
-          if (smem_ok(dst - sbase + e * 128, 4)) st_cluster_f32(cdst + e * 128, __uint_as_float(r[e]));
+          if (smem_ok(dst - sbase + e * 128, 4)) st_async_b32(cdst + e * 128, r[e], cbar);
       }
     }
     if (splits == 1 && c_tma) {
@@ -813,17 +832,24 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   uint32_t stg_stride = static_cast<uint32_t>(args.stg_blocks) * kBlockBytes;
   asm volatile("" : "+r"(n_cols), "+l"(c_out), "+r"(stg_stride));
   tc_fence_before_sync();
-  if (splits > 1 || kShare) cluster_sync_all(); else __syncthreads();
+  if constexpr (kShare) {
+    cluster_sync_all();  // no CTA leaves while a peer may still push operands into it
+  } else {
+    if (splits > 1 && warp < 2) cluster_wait_acquire();  // (their arrival at the start)
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
     tmem_dealloc(tmem_base, args.tmem_cols);
   }
   if (warp >= 2 && splits > 1) {
     // ------------------------------------------------ sum the owned blocks over the splits, store bf16
-    // Only local shared memory is read from here on, so no CTA waits for its
-    // peers before exiting.
+    // An owner waits until its peers' partials have all landed (red_bar
+    // counts their bytes); its own were stored before the CTA barrier above.
+    // Nothing else is waited for: a CTA that owns no block exits at once.
     const int tid = threadIdx.x - 64;
     const int mine = (valid_blocks - static_cast<int>(rank) + splits - 1) / splits;
+    if (mine > 0 && !mbar_wait(red_bar, 0, timeout) && tid == 0) report_error(args.err, kErrWaitReduce);
     const int n_base = n_tile * kTileN;
     const bool vec_ok = (n_cols % 4) == 0;
     const uint32_t stg = sbase + args.stg_off;  // shared-window address: ld.shared, not generic loads
@@ -834,11 +860,20 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       if (m >= m_valid) continue;
       const uint32_t off = lb * kBlockBytes + row * 128 + c4 * 16;
       if (!smem_ok(args.stg_off + (splits - 1) * stg_stride + off, 16)) continue;
-      float4 acc = ld_shared_f4(stg + off);
-      for (int src = 1; src < splits; ++src) {
-        const float4 p = ld_shared_f4(stg + src * stg_stride + off);
-        acc.x += p.x; acc.y += p.y; acc.z += p.z; acc.w += p.w;
-      }
+      // every source's loads first, then the sum in rank order (deterministic)
+      float4 part[kMaxSplits];
+#pragma unroll
+      for (int src = 0; src < kMaxSplits; ++src)
+        if (src < splits) part[src] = ld_shared_f4(stg + src * stg_stride + off);
+      float4 acc = part[0];
+#pragma unroll
+      for (int src = 1; src < kMaxSplits; ++src)
+        if (src < splits) {
+          acc.x += part[src].x;
+          acc.y += part[src].y;
+          acc.z += part[src].z;
+          acc.w += part[src].w;
+        }
       const int64_t gm = static_cast<int64_t>(m_base) + m;
       const int gn = n_base + (bi & 3) * 32 + c4 * 4;
       __nv_bfloat16* dst = c_out + gm * n_cols + gn;
@@ -964,7 +999,7 @@ GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t 
   L.stg_blocks = splits > 1 ? static_cast<int32_t>(ceil_div(blocks, splits)) : 0;  // no split: no staging
   L.bar_off = L.stg_off + static_cast<uint32_t>(splits * L.stg_blocks) * kBlockBytes;
   const uint32_t nbuf = st > static_cast<uint32_t>(L.abf_ring) ? st : static_cast<uint32_t>(L.abf_ring);
-  L.total = L.bar_off + (3 * st + 2 * nbuf + 1) * 8 + 16;
+  L.total = L.bar_off + (3 * st + 2 * nbuf + 2) * 8 + 16;  // ... accum, red_bar; tmem slot + abort flag
   return L;
 }
 

@@ -21,6 +21,7 @@ enum DeviceError : uint32_t {
   kErrBadPlan = 1u << 6,     // launch geometry disagrees with the kernel
   kErrWaitFlag = 1u << 7,    // a wait on another CTA's completion counter (multi-layer kernel)
   kErrBounds = 1u << 8,      // checked build: an index outside its buffer (the access was skipped)
+  kErrWaitReduce = 1u << 9,  // split-K owner waiting for its peers' partial sums
 };
 
 __device__ __forceinline__ void report_error(uint32_t* word, uint32_t bits) {
@@ -387,6 +388,15 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync_all() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
                    : "memory");
+}
+
+// The two halves of cluster_sync_all, for a barrier whose arrival and wait are
+// far apart (every thread of the CTA executes each, warp-uniformly).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
 // This CTA's coordinates inside its thread-block cluster.
