@@ -189,8 +189,9 @@ size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // The fused entry quantizes A once into a workspace and runs the GEMM on
 // codes when M is large enough that re-reading bf16 A in every N tile costs
-// more than the extra launch (measured on GB300: from M = 64 on).
-bool two_pass_wanted(int64_t M) { return M >= 64; }
+// more than the extra launch (measured on GB300: from M = 64 on), unless a
+// tuned single-kernel plan for the exact shape measured faster.
+bool two_pass_wanted(int64_t M, int64_t N, int64_t K) { return M >= 64 && !tuned_single_kernel(M, N, K); }
 
 size_t two_pass_workspace(int64_t M, int64_t K) {
   return align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2)) +
@@ -321,7 +322,7 @@ mxfp4_status_t prepare_quant_gemm(const void* A, int64_t lda, const void* Bpacke
   mxfp4_status_t st = check_mnk(M, N, K);
   if (st != MXFP4_OK) return st;
   if (ws_bytes > 0 && ws == nullptr) return MXFP4_ERR_INVALID_ARG;
-  q->two_pass = ws_bytes > 0 && two_pass_wanted(M);
+  q->two_pass = ws_bytes > 0 && two_pass_wanted(M, N, K);
   if (!q->two_pass) return prepare_gemm(A, lda, nullptr, Bpacked, C, M, N, K, true, nullptr, c_host, &q->gemm);
   if (ws_bytes < two_pass_workspace(M, K)) return MXFP4_ERR_WORKSPACE_TOO_SMALL;
   if (!aligned16(ws)) return MXFP4_ERR_MISALIGNED;
@@ -616,7 +617,7 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
 
 size_t mxfp4_workspace_bytes(int64_t M, int64_t N, int64_t K) {
   if (check_mnk(M, N, K) != MXFP4_OK) return 0;
-  return two_pass_wanted(M) ? two_pass_workspace(M, K) : 0;
+  return two_pass_wanted(M, N, K) ? two_pass_workspace(M, K) : 0;
 }
 
 mxfp4_status_t mxfp4_gemm(const void* Aq, const void* As, const void* Bpacked, void* C, int64_t M,
@@ -677,7 +678,7 @@ mxfp4_status_t mxfp4_gemm_plan(int64_t M, int64_t N, int64_t K, int fused, mxfp4
   if (st != MXFP4_OK) return st;
   const DeviceInfo* dev = current_device(&st);
   if (dev == nullptr) return st;
-  const bool two_pass = fused != 0 && two_pass_wanted(M);
+  const bool two_pass = fused != 0 && two_pass_wanted(M, N, K);
   cached_default_plan(M, N, K, fused != 0 && !two_pass, dev->prop, plan);
   plan->two_pass = two_pass ? 1 : 0;
   return plan->threads == 0 ? MXFP4_ERR_UNSUPPORTED_SHAPE : MXFP4_OK;

@@ -102,6 +102,9 @@ struct GemmLayout {
   int32_t stg_blocks;
 };
 GemmLayout gemm_layout(int block_m, int stages, int splits, bool fused, int64_t M, int abf_ring);
+// True when the tuned plans hold a single fused-kernel plan for this exact
+// shape (the fused entry then takes no two-pass route, whatever M).
+bool tuned_single_kernel(int64_t M, int64_t N, int64_t K);
 // The fused kernel's bf16 buffer count for a finished plan (0 unfused).
 int abf_ring_for(const mxfp4_plan_t& p, bool fused, int64_t M, const cudaDeviceProp& prop);
 

@@ -146,8 +146,9 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
  *            mxfp4_gemm needs none: it accepts and ignores any ws, ws_bytes.
  *            mxfp4_quant_gemm chooses its route by them:
  *              - ws_bytes == 0: the single fused kernel, for every M;
- *              - ws_bytes > 0 and M >= 64 (where mxfp4_workspace_bytes() is
- *                non-zero): the two-pass route -- A quantized into the
+ *              - ws_bytes > 0 and mxfp4_workspace_bytes(M, N, K) non-zero
+ *                (M >= 64, except the shapes whose tuned plan is the single
+ *                kernel): the two-pass route -- A quantized into the
  *                workspace by mxfp4_quantize, then the GEMM on the codes, two
  *                launches that overlap; faster than the single kernel once M
  *                is large, because that kernel re-reads the bf16 activation
@@ -155,7 +156,7 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
  *                mxfp4_workspace_bytes(M, N, K) returns
  *                MXFP4_ERR_WORKSPACE_TOO_SMALL, a ws that is not 16-byte
  *                aligned MXFP4_ERR_MISALIGNED (nothing launched);
- *              - ws_bytes > 0 and M < 64: the single fused kernel (ws unused);
+ *              - ws_bytes > 0 otherwise: the single fused kernel (ws unused);
  *              - ws == NULL with ws_bytes > 0: MXFP4_ERR_INVALID_ARG.
  *            The workspace is overwritten; calls that share one must be
  *            ordered.

@@ -62,6 +62,9 @@ def test_packed_weight_bytes_layout(lib):
     assert lib.mxfp4_workspace_bytes(64, 7168, 2048) == 64 * 1024 + 64 * 64
     assert lib.mxfp4_workspace_bytes(100, 128, 96) == 4864 + 512
     assert lib.mxfp4_workspace_bytes(64, 128, 40) == 0
+    # a shape whose tuned plan is the single fused kernel even at M = 64
+    assert lib.mxfp4_workspace_bytes(64, 3072, 1536) == 0
+    assert lib.mxfp4_workspace_bytes(65, 3072, 1536) > 0
 
 
 def test_argument_checks_launch_nothing(lib):
