@@ -617,6 +617,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       int kdim = args.K;
       asm volatile("" : "+l"(a_glob), "+l"(lda_bytes), "+r"(kdim));
       D tiles;
+      int s = 0, round = 0;  // stage and reuse round of the next K tile
       for (int g0 = 0; g0 < kt_count; g0 += group) {
         const int n = min(group, kt_count - g0);
         tiles.load(a_glob, lda_bytes, m_base, m_valid, kdim, kt_begin + g0, n, tid, args.M, args.err);
@@ -624,21 +625,28 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
           grid_launch_dependents();
           triggered = true;
         }
+        bool stop = false;
 #pragma unroll
         for (int j = 0; j < D::kGroup; ++j) {
           if (j >= n) break;
-          const int i = g0 + j, s = i % stages, round = i / stages;
-          if (round > 0 && !*abort_flag && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
-            report_error(args.err, kErrWaitEmpty);
-            *abort_flag = 1u;
+          if (round > 0) {  // a reused stage: wait until its MMAs are done
+            if (!*abort_flag && !mbar_wait(empty(s), (round - 1) & 1, timeout)) {
+              report_error(args.err, kErrWaitEmpty);
+              *abort_flag = 1u;
+            }
+            stop = __any_sync(0xFFFFFFFFu, *abort_flag != 0u);  // warp-uniform: the shuffles need every lane
+            if (stop) break;
           }
-          if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;  // warp-uniform: the shuffles need every lane
           tiles.quantize(j, smem + a_off + s * C::kATileBytes, smem + sfa_off + s * C::kSfaStageBytes, tid, m_valid);
           fence_proxy_async_smem();  // this thread's generic stores, visible to tcgen05
           __syncwarp();
           if (lane == 0) mbar_arrive(full_a(s));
+          if (++s == stages) {
+            s = 0;
+            ++round;
+          }
         }
-        if (__any_sync(0xFFFFFFFFu, *abort_flag != 0u)) break;
+        if (stop) break;
       }
     }
     for (int i = 0, s = 0, round = 0, r = 0, round_a = 0; !kShare && !kDirect && i < kt_count;
