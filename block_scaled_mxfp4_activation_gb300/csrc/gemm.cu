@@ -288,7 +288,10 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   if (threadIdx.x == 0) {
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_w(s), 1);
-      mbar_init(full_a(s), kShare ? 1 : C::kAWarps);  // one arrival per producer warp; kShare: own arrival + bytes
+      // fused: one arrival per producer warp (kShare: its own arrival + the
+      // pushed bytes); unfused: the producer warps' scale arrivals plus the
+      // codes' TMA (its arrival + bytes), so the MMA issuer waits on one barrier
+      mbar_init(full_a(s), kShare ? 1 : kFused ? C::kAWarps : C::kAWarps + 1);
       mbar_init(empty(s), 1);
     }
     if constexpr (kShare) {
@@ -374,7 +377,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     // unfused into stage s
     auto issue_a = [&](int i, int s) {
       const int kt = kt_begin + i;
-      const uint32_t bar = full_in(s);
+      const uint32_t bar = kFused ? full_in(s) : full_a(s);
       if constexpr (kFused) {
         const uint32_t dst = sbase + args.abf_off + s * args.abf_stage_bytes;
         if (leader) {
@@ -459,7 +462,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     }
     for (int r = 0; r < ring_a && r < issued_a; ++r) {
       const uint32_t parity = ((r + ring_a * ((issued_a - 1 - r) / ring_a)) / ring_a) & 1;
-      if (!mbar_wait(full_in(r), parity, timeout) && leader) report_error(args.err, kErrWaitDrain);
+      if (!mbar_wait(kFused ? full_in(r) : full_a(r), parity, timeout) && leader) report_error(args.err, kErrWaitDrain);
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -655,12 +658,13 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         report_error(args.err, kErrWaitEmpty);
         *abort_flag = 1u;
       }
-      // fused: the tile's bf16 buffer r; unfused: the codes, in stage s
-      if (!*abort_flag && !mbar_wait(kFused ? full_in(r) : full_in(s), (kFused ? round_a : round) & 1, timeout)) {
+      // fused: the tile's bf16 buffer r.  Unfused: nothing to wait for -- the
+      // codes' TMA completes on full_a(s) itself, beside these warps' scales.
+      if (kFused && !*abort_flag && !mbar_wait(full_in(r), round_a & 1, timeout)) {
         report_error(args.err, kErrWaitTma);
         *abort_flag = 1u;
       }
-      if (!triggered) {  // the activation tile has landed: the next grid may start
+      if (!triggered) {  // fused: the activation tile has landed; the next grid may start
         grid_launch_dependents();
         triggered = true;
       }
