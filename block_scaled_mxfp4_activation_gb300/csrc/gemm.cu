@@ -1149,16 +1149,18 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // a split runs in sequence costs ~250 ns (operand loads, tensor-memory scale
 // copies, four MMAs) plus, on the fused kernel, ~200 ns per 32 activation rows
 // it quantizes (so 16-row tiles halve it: at M = 32 two CTAs of 16 rows beat
-// one of 32); a K split adds ~700 ns for the cluster reduction (measured on
-// GB300 with graph-replayed calls).  Among plans that run in one wave, those
-// whose shared memory lets two CTAs share an SM come first: the next call's
-// CTAs then start early beside this call's (programmatic launch), and losing
-// that overlap costs more than any stage depth gains (K = 7168, 7 splits: 2
-// stages 5.6 us, 4 stages with one CTA per SM 10.0 us).  Candidates: block_m
-// from the smallest tile that holds M (capped at 256) down to a quarter of it;
-// every split count that leaves no split empty; 1 to 6 stages (at most the
-// split's K tiles).  Ties prefer the larger block_m (fewer re-reads of the
-// weights), then the larger stage count, then fewer splits.
+// one of 32); a K split adds ~700 ns for the reduction; a split with more K
+// tiles than stages adds ~1 us per reload, divided by the stages in flight
+// (measured on GB300 with graph-replayed calls).  Among plans that run in one
+// wave, those that leave room for the next call's CTAs beside this call's
+// (twice the CTAs fit at the plan's CTAs per SM) come first: the next call
+// then starts early under programmatic launch, and losing that overlap costs
+// more than a deeper stage ring gains (K = 7168, 7 splits: 2 stages 5.6 us,
+// 4 stages with one CTA per SM 10.0 us).  Candidates: block_m from the
+// smallest tile that holds M (capped at 128) down to a quarter of it; every
+// split count that leaves no split empty; 1 to 6 stages (at most the split's
+// K tiles).  Ties prefer the larger block_m (fewer re-reads of the weights),
+// then the larger stage count, then fewer splits.
 // Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
 // the estimate is not (keyed on the shape): sweeps of block_m x splits x
 // stages x share, graph-replayed calls with rotating operands.  `fused` is the
@@ -1194,7 +1196,11 @@ bool tuned_single_kernel(int64_t M, int64_t N, int64_t K) {
 static int64_t plan_cost_ns(const mxfp4_plan_t& p, int64_t M, bool fused) {
   const int64_t rows = M < p.block_m ? M : p.block_m;
   const int64_t tile = 250 + (fused ? 200 * rows / 32 : 0);
-  return p.k_tiles_per_split * tile + (p.splits > 1 ? 700 : 0);
+  const int64_t tiles = p.k_tiles_per_split;
+  // a stage reloaded `tiles - stages` times, each reload waiting for the MMAs
+  // of the tile before it: ~1 us of load latency, shared by the stages in flight
+  const int64_t refill = tiles > p.stages ? (tiles - p.stages) * 1000 / p.stages : 0;
+  return tiles * tile + (p.splits > 1 ? 700 : 0) + refill;
 }
 
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
@@ -1216,7 +1222,9 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
       return;
     }
   }
-  const int bm0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : M <= 128 ? 128 : 256;
+  // (block_m 256 measured slower than 128 at every M = 256 shape swept: its
+  // MMAs and operand tiles cost more than the weight re-reads they save)
+  const int bm0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
   const int64_t k_tiles = ceil_div(K, kTileK);
   const int64_t cap = 2 * static_cast<int64_t>(prop.multiProcessorCount);
   int64_t best[6] = {-1, 0, 0, 0, 0, 0};
@@ -1233,12 +1241,14 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
         const int64_t clusters = static_cast<int64_t>(q.grid_y) * q.grid_z;
         const int64_t ctas = clusters * splits;
         const int64_t one_wave = ctas <= cap && clusters <= active_clusters(q, fused) ? 1 : 0;
-        // two CTAs per SM leave room for the next call's CTAs to start early
-        const int64_t two_per_sm =
+        // the next call's CTAs can start beside this call's (programmatic
+        // launch) when twice the CTAs fit on the device at this plan's CTAs per SM
+        const int64_t per_sm =
             2 * (static_cast<int64_t>(q.smem_bytes) + prop.reservedSharedMemPerBlock) <= prop.sharedMemPerMultiprocessor
-                ? 1
-                : 0;
-        const int64_t score[6] = {one_wave, two_per_sm, one_wave ? -plan_cost_ns(q, M, fused) : -ctas, bm, st, -splits};
+                ? 2
+                : 1;
+        const int64_t room_for_next = 2 * ctas <= per_sm * static_cast<int64_t>(prop.multiProcessorCount) ? 1 : 0;
+        const int64_t score[6] = {one_wave, room_for_next, one_wave ? -plan_cost_ns(q, M, fused) : -ctas, bm, st, -splits};
         bool better = false;
         for (int i = 0; i < 6; ++i) {
           if (score[i] != best[i]) {
