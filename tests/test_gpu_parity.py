@@ -430,8 +430,10 @@ def test_gemm_full_size_every_element(oracle_mod, name):
     bq, bs, W = quantized_weight(oracle_mod, B)
     aq, as_ = oracle_mod.quantize(A)
     Ad = A.cuda()
-    C = mx.quant_gemm(Ad, W).cpu()
-    C_single = mx.quant_gemm(Ad, W, workspace=torch.empty(0, dtype=torch.uint8, device="cuda")).cpu()
+    ws_bytes = mx.workspace_bytes(w.M, w.N, w.K)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if ws_bytes else None
+    C = mx.quant_gemm(Ad, W, workspace=ws).cpu()  # the route the library picks given what it asks for
+    C_single = mx.quant_gemm(Ad, W).cpu()
     Aq, As = mx.quantize(Ad)
     C_unfused = mx.gemm(Aq, As, W).cpu()
     assert np.array_equal(Aq.cpu().numpy(), aq) and np.array_equal(As.cpu().numpy(), as_)
@@ -456,22 +458,30 @@ def extra_shapes():
 def test_gemm_extra_shapes(oracle_mod, M, N, K, seed):
     """Every output element against the oracle (sampled elements above 4e9
     multiply-adds, where the full oracle GEMM would take minutes), default route;
-    codes and scales bit-exact."""
+    codes and scales bit-exact.  Both routes where the library offers two: the
+    single fused kernel, and the two-pass route given the workspace it asks for."""
     A, B = workloads.make_random(M, N, K, seed=seed)
     bq, bs, W = quantized_weight(oracle_mod, B)
     aq, as_ = oracle_mod.quantize(A)
     Ad = A.cuda()
-    C = mx.quant_gemm(Ad, W).cpu()
+    results = {"single fused kernel": mx.quant_gemm(Ad, W).cpu()}
+    ws_bytes = mx.workspace_bytes(M, N, K)
+    if ws_bytes:
+        ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+        results["two-pass route"] = mx.quant_gemm(Ad, W, workspace=ws).cpu()
     Aq, As = mx.quantize(Ad)
     assert np.array_equal(Aq.cpu().numpy(), aq) and np.array_equal(As.cpu().numpy(), as_)
     if M * N * K <= 4e9:
-        check_close(C, gemm_full(oracle_mod, aq, as_, bq, bs), f"{M}x{N}x{K}")
+        c64 = gemm_full(oracle_mod, aq, as_, bq, bs)
+        for what, C in results.items():
+            check_close(C, c64, f"{M}x{N}x{K} {what}")
     else:
         rng = np.random.default_rng(seed)
         ms = np.concatenate([rng.integers(0, M, 4000), np.full(64, M - 1), np.zeros(64, np.int64)])
         ns = np.concatenate([rng.integers(0, N, 4000), N - 1 - np.arange(64), np.arange(64)])
         c64, _ = oracle_mod.gemm_sampled(aq, as_, bq, bs, ms, ns)
-        check_close(C[ms, ns], c64, f"{M}x{N}x{K} sampled")
+        for what, C in results.items():
+            check_close(C[ms, ns], c64, f"{M}x{N}x{K} {what}, sampled")
 
 
 @pytest.mark.parametrize("pinned", [True, False])
