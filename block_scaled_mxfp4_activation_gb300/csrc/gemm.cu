@@ -13,21 +13,24 @@
 //     operand (N = block_m), so a handful of tokens still fills the MMA;
 //   - warp 0 issues every load of the CTA at once with TMA: per 256-wide K
 //     tile, the 128 x 128-byte box of weight codes (128-byte swizzle), the
-//     tile's 1 KB of pre-arranged weight scales (bulk copy) and the activation
-//     tile -- bf16 for the fused entry, codes straight into the MMA operand's
-//     swizzled layout for the unfused one;
-//   - warps 2.. quantize the staged bf16 activation tile in shared memory (or
-//     place the pre-quantized scales), writing codes in the operand's swizzled
-//     layout and scales in the tensor-memory scale-chunk layout;
-//   - warp 1 moves both scale sets to tensor memory (tcgen05.cp) and issues
-//     four K = 64 block-scaled MMAs per stage into an fp32 accumulator in
-//     tensor memory;
+//     tile's 1 KB of pre-arranged weight scales (bulk copy) and, except on
+//     the direct path, the activation tile -- bf16 for the fused entry, codes
+//     straight into the MMA operand's swizzled layout for the unfused one;
+//   - warps 2.. quantize the activation (fused: at block_m 16 and 32 loaded
+//     straight from global memory into registers, else from the bf16 tile
+//     staged in shared memory) or place the pre-quantized scales, writing
+//     codes in the operand's swizzled layout and scales in the tensor-memory
+//     scale-chunk layout;
+//   - one lane of warp 1 moves both scale sets to tensor memory (tcgen05.cp)
+//     and issues four K = 64 block-scaled MMAs per stage into an fp32
+//     accumulator in tensor memory;
 //   - without a K split, the accumulator leaves as bf16 through a tile in
 //     shared memory and one TMA tensor store;
 //   - K splits of one output tile form a thread-block cluster: each CTA
-//     pushes its fp32 partial blocks to their owners' shared memory and every
-//     owner sums its blocks over the splits in a fixed order (deterministic,
-//     no global workspace, no second kernel), then stores 8 bytes per thread.
+//     pushes its fp32 partial blocks into their owners' shared memory with
+//     st.async, counted on the owner's barrier, and every owner sums its
+//     blocks over the splits in a fixed order (deterministic, no global
+//     workspace, no second kernel), then stores 8 bytes per thread.
 //
 // Back-to-back calls overlap through programmatic dependent launch: the next
 // call's CTAs set up and load their weights into shared memory while this one
