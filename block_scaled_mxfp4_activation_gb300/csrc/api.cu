@@ -361,7 +361,10 @@ struct ChainGeometry {
   size_t counters = 0, n_counters = 0, total = 0;
 };
 
-int chain_block_m(int64_t M) { return M <= 16 ? 16 : M <= 32 ? 32 : 64; }
+// 16-row tiles up to M = 32 (twice the items of 32-row ones, each quantizing
+// half the rows: 32 x 4096 x 512 up/down chain 4.49 -> 4.26 us per layer),
+// 64-row tiles above (32-row ones measured slower at M = 64).
+int chain_block_m(int64_t M) { return M <= 32 ? 16 : 64; }
 
 void chain_geometry(int64_t M, int64_t K, int L, const int64_t* N, ChainGeometry* g) {
   g->bm = chain_block_m(M);

@@ -158,7 +158,7 @@ def chain_workspace_expected(M: int, K: int, Ns: list[int]) -> int:
     """The multi-layer workspace, restated: per layer codes, scale chunks and
     split-K partials (for up to min(8, K tiles) splits), then the counters."""
     a256 = lambda x: -(-x // 256) * 256
-    bm = 16 if M <= 16 else 32 if M <= 32 else 64
+    bm = 16 if M <= 32 else 64
     mt = -(-M // bm)
     total, counters, k = 0, 0, K
     for n in Ns:
