@@ -288,6 +288,43 @@ def test_gemm_random_shapes(oracle_mod, M, N, K):
         check_close(C, c64, f"{what} {M}x{N}x{K}")
 
 
+def test_random_plans_against_oracle(oracle_mod):
+    """60 seeded random shapes (M 1-79, N 1-1199, K a multiple of 32 up to
+    3168), each under three random plans (block_m 16/32/64, 1-8 K splits, 0-3
+    stages): the fused and the unfused kernel bit-identical under each plan,
+    every plan within the tolerance of the oracle on every element, and the
+    two routes of the default entry as well."""
+    rng = np.random.default_rng(20251203)
+    ran = 0
+    for c in range(60):
+        M, N, K = int(rng.integers(1, 80)), int(rng.integers(1, 1200)), 32 * int(rng.integers(1, 100))
+        A, B = workloads.make_random(M, N, K, seed=c)
+        bq, bs, W = quantized_weight(oracle_mod, B)
+        aq, as_ = oracle_mod.quantize(A)
+        c64 = gemm_full(oracle_mod, aq, as_, bq, bs)
+        Ad = A.cuda()
+        Aq, As = mx.quantize(Ad)
+        for _ in range(3):
+            plan = {"block_m": int(rng.choice([16, 32, 64])), "splits": int(rng.integers(1, 9)),
+                    "stages": int(rng.integers(0, 4))}
+            try:
+                Cf = mx.gemm_with_plan(Ad, None, W, plan, True)
+                Cu = mx.gemm_with_plan(Aq, As, W, plan, False)
+            except mx.MXFP4Error as e:
+                assert e.status == 1, (M, N, K, plan)  # a plan that does not fit this shape
+                continue
+            ran += 1
+            assert torch.equal(Cf, Cu), f"fused != unfused, {M}x{N}x{K} {plan}"
+            check_close(Cf, c64, f"{M}x{N}x{K} {plan}")
+        ws_bytes = mx.workspace_bytes(M, N, K)
+        check_close(mx.quant_gemm(Ad, W), c64, f"{M}x{N}x{K} default, single kernel")
+        if ws_bytes:
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda")
+            check_close(mx.quant_gemm(Ad, W, workspace=ws), c64, f"{M}x{N}x{K} default, two-pass")
+    assert ran >= 60
+    assert mx.device_error(reset=True) == 0
+
+
 def test_gemm_every_plan_agrees(oracle_mod):
     M, N, K = 40, 384, 2048
     A, B = workloads.make_random(M, N, K, seed=99)
