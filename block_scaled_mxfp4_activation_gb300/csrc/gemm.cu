@@ -499,7 +499,11 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       int mma_k = args.K;
       asm volatile("" : "+r"(mma_a_off), "+r"(mma_sfa_off), "+r"(mma_k));  // parameters read before the waits
       bool alive = true;
-      for (int i = 0; i < pre && alive; ++i) alive = weight_scales(i, 0);
+      // weights loaded after the grid wait arrive stage by stage: copy only the
+      // first stage's scales up front and each later one just before its tile,
+      // so tile 0 never waits for the last stage's weights
+      const int pre_copy = args.weights_early ? pre : min(pre, 1);
+      for (int i = 0; i < pre_copy && alive; ++i) alive = weight_scales(i, 0);
       // stage 0's descriptors; stage s adds s tiles (the address field counts 16-byte units)
       const uint64_t a_desc0 = smem_desc(sbase, 16, 1024, 2);
       const uint64_t b_desc0 = smem_desc(sbase + mma_a_off, 16, 1024, 2);
@@ -511,7 +515,7 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
         const uint64_t a_desc = a_desc0 + static_cast<uint64_t>(s * (C::kBTileBytes >> 4));
         const uint64_t b_desc = b_desc0 + static_cast<uint64_t>(s * (C::kATileBytes >> 4));
         const int k0 = (kt_begin + i) * kTileK;
-        if (i >= stages && !weight_scales(s, round)) break;  // a reloaded stage
+        if (i >= pre_copy && !weight_scales(s, round)) break;  // a later or reloaded stage
         // (another role's abort shows up here as a wait that runs out)
         if (!mbar_wait(full_a(s), round & 1, timeout)) {
           report_error(args.err, kErrWaitA);
