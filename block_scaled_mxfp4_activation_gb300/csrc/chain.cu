@@ -249,12 +249,22 @@ __global__ void __launch_bounds__(kChainThreads, 2) chain_kernel(const __grid_co
                                      smem_desc(sbase + p.sfa_off + s * kChainATileSf + c * kSfChunkBytes, 128, 128, 0));
             const uint64_t a_desc = smem_desc(sbase + s * (kTileN * kTileKBytes), 16, 1024, 2);
             const uint64_t b_desc = smem_desc(sbase + p.a_off + s * kATileBytes, 16, 1024, 2);
+            // a whole K tile: four MMAs with compile-time operand offsets and no
+            // per-step bound (the issuing lane's instructions set the MMA rate)
+            const int steps = kt * kTileK + kTileK <= K ? 4 : (K - kt * kTileK + 63) / 64;
+            if (steps == 4) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              if (kt * kTileK + 64 * j >= K) break;
-              const uint32_t sid = (j & 1) * 2;
-              mma_mxf4(tmem_base, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>(sid), sfw_t + 4 * (j >> 1),
-                       sfa_t + 4 * (j >> 1), (first && j == 0) ? 0u : 1u);
+              for (int j = 0; j < 4; ++j)
+                mma_mxf4(tmem_base, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>((j & 1) * 2), sfw_t + 4 * (j >> 1),
+                         sfa_t + 4 * (j >> 1), (first && j == 0) ? 0u : 1u);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                if (j >= steps) break;
+                const uint32_t sid = (j & 1) * 2;
+                mma_mxf4(tmem_base, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>(sid), sfw_t + 4 * (j >> 1),
+                         sfa_t + 4 * (j >> 1), (first && j == 0) ? 0u : 1u);
+              }
             }
             tc_commit(empty(s));  // the stage is free once these MMAs have read it
           }

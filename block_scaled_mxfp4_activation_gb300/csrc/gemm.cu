@@ -530,16 +530,26 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
 #pragma unroll
         for (int c = 0; c < 2 * C::kRowChunks; ++c)
           tmem_cp_32x128b_warpx4(sfa_t + 4 * c, smem_desc(sfa_s + c * kSfChunkBytes, 128, 128, 0));
+        if (nacc == 1 && k0 + kTileK <= mma_k) {
+          // a whole K tile into the one accumulator: four MMAs whose operands
+          // differ only by compile-time offsets (the issuing lane's own
+          // instruction stream sets the MMA rate at these tile sizes)
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          if (k0 + 64 * j >= mma_k) break;
-          const uint32_t sid = (j & 1) * 2;
-          // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 -> +2)
-          // K step g = 4i + j accumulates into tile g % nacc: nacc independent
-          // chains the tensor core can overlap (summed in the epilogue)
-          const int g = 4 * i + j, acc = g & (nacc - 1);
-          mma_mxf4(tmem_base + acc * BM, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>(sid), sfw_t + 4 * (j >> 1),
-                   sfa_t + 4 * C::kRowChunks * (j >> 1), g >= nacc);
+          for (int j = 0; j < 4; ++j)
+            mma_mxf4(tmem_base, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>((j & 1) * 2), sfw_t + 4 * (j >> 1),
+                     sfa_t + 4 * C::kRowChunks * (j >> 1), (i | j) != 0);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (k0 + 64 * j >= mma_k) break;
+            const uint32_t sid = (j & 1) * 2;
+            // +32 bytes of K per step inside the 128-byte swizzle row (>> 4 -> +2)
+            // K step g = 4i + j accumulates into tile g % nacc: nacc independent
+            // chains the tensor core can overlap (summed in the epilogue)
+            const int g = 4 * i + j, acc = g & (nacc - 1);
+            mma_mxf4(tmem_base + acc * BM, a_desc + 2 * j, b_desc + 2 * j, mxf4_idesc<BM>(sid), sfw_t + 4 * (j >> 1),
+                     sfa_t + 4 * C::kRowChunks * (j >> 1), g >= nacc);
+          }
         }
         if (i + stages < kt_count) tc_commit(empty(s));  // frees the stage when these MMAs finish
       }
