@@ -373,6 +373,29 @@ def test_gemm_independent_accumulators(oracle_mod, accumulators):
             check_close(C, c64, f"plan {plan} fused={fused}")
 
 
+@pytest.mark.parametrize("K", [32, 256, 288, 480, 512, 544, 1024 + 224])
+def test_gemm_whole_and_ragged_k_tiles(oracle_mod, K):
+    # the MMA issue takes a whole 256-wide K tile in one unchecked step and a
+    # ragged last tile (K % 256 = 32 .. 224) step by step; one accumulator uses
+    # the whole-tile step, two use the checked loop: every mix against the oracle
+    M, N = 24, 260
+    A, B = workloads.make_random(M, N, K, seed=K)
+    bq, bs, W = quantized_weight(oracle_mod, B)
+    _, _, c64, _ = oracle_mod.quant_gemm(A, bq, bs)
+    Ad = A.cuda()
+    Aq, As = mx.quantize(Ad)
+    kt = -(-K // 256)
+    for bm, splits, stages, acc in ((16, 1, 0, 1), (32, 1, 2, 1), (64, 1, 1, 1), (16, min(2, kt), 0, 2),
+                                    (64, kt, 0, 1)):
+        plan = {"block_m": bm, "splits": splits, "stages": stages, "accumulators": acc}
+        for fused in (True, False):
+            C = mx.gemm_with_plan(Ad if fused else Aq, None if fused else As, W, plan, fused)
+            check_close(C, c64, f"K={K} plan {plan} fused={fused}")
+    # the multi-layer kernel's issue loop (same split of whole and ragged tiles)
+    outs = mx.quant_gemm_chain(Ad, [W])
+    check_close(outs[-1], c64, f"K={K} multi-layer launch")
+
+
 def test_gemm_deterministic_and_graph_replay(oracle_mod):
     M, N, K = 16, 2112, 7168
     A, B = workloads.make_random(M, N, K, seed=5, b_std=0.02, outlier_frac=0.01)
