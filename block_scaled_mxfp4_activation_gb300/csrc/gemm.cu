@@ -289,6 +289,9 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
   (void)smem_ok;
 
   if (threadIdx.x == 0) {
+    prefetch_tmap(&tmap_b);
+    prefetch_tmap(&tmap_a);
+    if (args.c_tma) prefetch_tmap(&tmap_c);
     for (int s = 0; s < stages; ++s) {
       mbar_init(full_w(s), 1);
       // fused: one arrival per producer warp (kShare: its own arrival + the
@@ -322,11 +325,25 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
     }
     *abort_flag = 0u;
     fence_mbar_init();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tmap(&tmap_b);
-    prefetch_tmap(&tmap_a);
-    if (args.c_tma) prefetch_tmap(&tmap_c);
+    if (kFused && args.weights_early) {
+      // fused: the weights of the first stages, issued by the thread that has
+      // just initialised their barriers, before the CTA's set-up (tensor
+      // memory, CTA barrier) rather than after it: they are the first operand
+      // the call waits for when it starts just ahead of its grid wait.  (The
+      // pre-quantized kernel keeps them behind its set-up: issued earlier they
+      // compete with the quantize pass that runs just before it, 6.03 -> 6.20
+      // us per call at M=64.)
+      const uint64_t policy_w = policy_evict_first();
+      for (int i = 0; i < stages && i < kt_count; ++i) {
+        const int kt = kt_begin + i;
+        const uint32_t bar = full_w(i);
+        mbar_arrive_expect_tx(bar, C::kBTileBytes + kSfTileBytes);
+        tma_load_2d(sbase + i * C::kBTileBytes, &tmap_b, kt * kTileKBytes, n_tile * kTileN, bar, policy_w);
+        bulk_load(sbase + args.sfw_off + i * kSfTileBytes,
+                  args.b_sf + (static_cast<size_t>(n_tile) * args.k_tiles + kt) * kSfTileBytes, kSfTileBytes, bar,
+                  policy_w);
+      }
+    }
   }
   if (warp == 1) {
     tmem_alloc(smem_u32(tmem_slot), args.tmem_cols);
@@ -396,7 +413,8 @@ __global__ void __launch_bounds__(TileCfg<BM, kFused>::kThreads, 2)
       }
     };
     if (args.weights_early) {
-      for (int i = 0; i < pre; ++i) issue_w(i, i);
+      if constexpr (!kFused)
+        for (int i = 0; i < pre; ++i) issue_w(i, i);  // (fused: thread 0 issued them during set-up)
     } else {
       for (int i = 0; i < kt_count; ++i) {
         const int kt = kt_begin + i;
