@@ -15,7 +15,10 @@
 //     tile, the 128 x 128-byte box of weight codes (128-byte swizzle), the
 //     tile's 1 KB of pre-arranged weight scales (bulk copy) and, except on
 //     the direct path, the activation tile -- bf16 for the fused entry, codes
-//     straight into the MMA operand's swizzled layout for the unfused one;
+//     straight into the MMA operand's swizzled layout for the unfused one
+//     (fused, with weights loaded ahead of the grid wait: the first stages'
+//     weights are issued by thread 0 as soon as it has initialised their
+//     barriers, before the rest of the set-up);
 //   - warps 2.. quantize the activation (fused: at block_m 16 and 32 loaded
 //     straight from global memory into registers, else from the bf16 tile
 //     staged in shared memory) or place the pre-quantized scales, writing
