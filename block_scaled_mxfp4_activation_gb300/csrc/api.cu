@@ -188,10 +188,18 @@ void cached_default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cuda
 size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
 // The fused entry quantizes A once into a workspace and runs the GEMM on
-// codes when M is large enough that re-reading bf16 A in every N tile costs
-// more than the extra launch (measured on GB300: from M = 64 on), unless a
-// tuned single-kernel plan for the exact shape measured faster.
-bool two_pass_wanted(int64_t M, int64_t N, int64_t K) { return M >= 64 && !tuned_single_kernel(M, N, K); }
+// codes when re-reading bf16 A in every 128-row N tile costs more than the
+// extra launch.  Measured on GB300: from M = 64 on, except while M <= 128 and
+// those re-reads (2MK bytes per N tile) stay within ~5 MiB -- 128x4096x512
+// (4 MiB) 3.55 us in one kernel against 4.1 in two, 64x3072x1536 (4.5 MiB)
+// 4.4 against 5.0, while 64x7168x2048 (14 MiB) takes 6.0 in two against 11 in
+// one -- and unless a tuned single-kernel plan for the exact shape measured
+// faster.
+constexpr int64_t kFusedRereadMax = int64_t(5) << 20;
+bool two_pass_wanted(int64_t M, int64_t N, int64_t K) {
+  if (M < 64 || tuned_single_kernel(M, N, K)) return false;
+  return M > 128 || 2 * M * K * ((N + 127) / 128) > kFusedRereadMax;
+}
 
 size_t two_pass_workspace(int64_t M, int64_t K) {
   return align256(static_cast<size_t>(M) * static_cast<size_t>(K / 2)) +

@@ -1230,6 +1230,9 @@ bool tuned_single_kernel(int64_t M, int64_t N, int64_t K) {
   return false;
 }
 
+// Lost overlap of a plan whose CTAs leave no room for the next call's beside them, in ns.
+constexpr int64_t kNoRoomNs = 500;
+
 // Estimated critical path of one CTA, in ns (see above).
 static int64_t plan_cost_ns(const mxfp4_plan_t& p, int64_t M, bool fused) {
   const int64_t rows = M < p.block_m ? M : p.block_m;
@@ -1238,7 +1241,9 @@ static int64_t plan_cost_ns(const mxfp4_plan_t& p, int64_t M, bool fused) {
   // a stage reloaded `tiles - stages` times, each reload waiting for the MMAs
   // of the tile before it: ~1 us of load latency, shared by the stages in flight
   const int64_t refill = tiles > p.stages ? (tiles - p.stages) * 1000 / p.stages : 0;
-  return tiles * tile + (p.splits > 1 ? 700 : 0) + refill;
+  // a K split's reduction grows with the rows it sums: ~700 ns at 16 rows,
+  // ~2 us at 128 (96x4096x1024: 4 splits of 128 rows 5.7 us, none of 64 rows 4.6)
+  return tiles * tile + (p.splits > 1 ? 700 + 10 * rows : 0) + refill;
 }
 
 void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceProp& prop,
@@ -1262,7 +1267,13 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
   }
   // (block_m 256 measured slower than 128 at every M = 256 shape swept: its
   // MMAs and operand tiles cost more than the weight re-reads they save)
-  const int bm0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  // The fused kernel quantizes tiles of 16 or 32 rows straight from global
+  // memory into registers; larger tiles are staged in shared memory and
+  // quantized there, which measured slower up to M = 128 (65x3072x1536:
+  // 32-row tiles 4.7 us, 128-row 6.6; 100x2112x1536 and 128x4096x512 also
+  // fastest at 32 rows)
+  int bm0 = M <= 16 ? 16 : M <= 32 ? 32 : M <= 64 ? 64 : 128;
+  if (fused && M <= 128 && bm0 > 32) bm0 = 32;
   const int64_t k_tiles = ceil_div(K, kTileK);
   const int64_t cap = 2 * static_cast<int64_t>(prop.multiProcessorCount);
   int64_t best[6] = {-1, 0, 0, 0, 0, 0};
@@ -1285,8 +1296,12 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
             2 * (static_cast<int64_t>(q.smem_bytes) + prop.reservedSharedMemPerBlock) <= prop.sharedMemPerMultiprocessor
                 ? 2
                 : 1;
-        const int64_t room_for_next = 2 * ctas <= per_sm * static_cast<int64_t>(prop.multiProcessorCount) ? 1 : 0;
-        const int64_t score[6] = {one_wave, room_for_next, one_wave ? -plan_cost_ns(q, M, fused) : -ctas, bm, st, -splits};
+        // (a plan without that room pays ~0.5 us of lost overlap on top of its
+        // estimate, rather than losing to every plan with room whatever the
+        // estimates: 256x2880x7168 12.6 us with 2 splits against 16.8 without)
+        const bool room_for_next = 2 * ctas <= per_sm * static_cast<int64_t>(prop.multiProcessorCount);
+        const int64_t cost = plan_cost_ns(q, M, fused) + (room_for_next ? 0 : kNoRoomNs);
+        const int64_t score[6] = {one_wave, 0, one_wave ? -cost : -ctas, bm, st, -splits};
         bool better = false;
         for (int i = 0; i < 6; ++i) {
           if (score[i] != best[i]) {

@@ -147,7 +147,8 @@ mxfp4_status_t mxfp4_unpack_weights(const void* Bpacked, int64_t N, int64_t K, v
  *            mxfp4_quant_gemm chooses its route by them:
  *              - ws_bytes == 0: the single fused kernel, for every M;
  *              - ws_bytes > 0 and mxfp4_workspace_bytes(M, N, K) non-zero
- *                (M >= 64, except the shapes whose tuned plan is the single
+ *                (M >= 64, except where M <= 128 and 2*M*K*ceil(N/128)
+ *                <= 5 MiB, and the shapes whose tuned plan is the single
  *                kernel): the two-pass route -- A quantized into the
  *                workspace by mxfp4_quantize, then the GEMM on the codes, two
  *                launches that overlap; faster than the single kernel once M

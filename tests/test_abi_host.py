@@ -60,11 +60,18 @@ def test_packed_weight_bytes_layout(lib):
     assert lib.mxfp4_workspace_bytes(16, 2112, 7168) == 0  # single fused kernel
     # from M = 64 on: room for the codes and scales of A, each rounded to 256 bytes
     assert lib.mxfp4_workspace_bytes(64, 7168, 2048) == 64 * 1024 + 64 * 64
-    assert lib.mxfp4_workspace_bytes(100, 128, 96) == 4864 + 512
+    assert lib.mxfp4_workspace_bytes(200, 128, 96) == 9728 + 768
     assert lib.mxfp4_workspace_bytes(64, 128, 40) == 0
-    # a shape whose tuned plan is the single fused kernel even at M = 64
+    # ... except while M <= 128 and the single kernel's bf16 re-reads,
+    # 2*M*K per 128-row N tile, stay within 5 MiB
+    mib5 = 5 << 20
+    for M, N, K in ((100, 128, 96), (128, 4096, 512), (65, 3072, 1536), (128, 2560, 1024), (64, 7168, 2048),
+                    (128, 2688, 1024), (129, 128, 96), (96, 7168, 7168)):
+        reread = 2 * M * K * (-(-N // 128))
+        two = M > 128 or reread > mib5
+        assert (lib.mxfp4_workspace_bytes(M, N, K) > 0) == two, (M, N, K, reread)
+    # a shape whose tuned plan is the single fused kernel at M = 64
     assert lib.mxfp4_workspace_bytes(64, 3072, 1536) == 0
-    assert lib.mxfp4_workspace_bytes(65, 3072, 1536) > 0
 
 
 def test_argument_checks_launch_nothing(lib):
@@ -101,11 +108,11 @@ def test_argument_checks_launch_nothing(lib):
     assert lib.mxfp4_gemm_plan(4, 128, 64, 1, None) == INVALID
     assert lib.mxfp4_device_error(None, 0, None) == INVALID
     # the fused entry's workspace: offered but too small for the two-pass route
-    # (M >= 64), offered as a null pointer, or misaligned
-    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 64, 128, 64, fake, 16, None) == WS_SMALL
-    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 64, 128, 64, None, 1 << 20, None) == INVALID
-    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 64, 128, 64, odd, 1 << 20, None) == MISALIGNED
-    assert lib.mxfp4_quant_gemm_host(fake, 64, fake, 64, fake, fake, fake, 64, 128, 64, fake, 16, None) == WS_SMALL
+    # (here M > 128), offered as a null pointer, or misaligned
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 200, 128, 64, fake, 16, None) == WS_SMALL
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 200, 128, 64, None, 1 << 20, None) == INVALID
+    assert lib.mxfp4_quant_gemm(fake, 64, fake, fake, 200, 128, 64, odd, 1 << 20, None) == MISALIGNED
+    assert lib.mxfp4_quant_gemm_host(fake, 64, fake, 64, fake, fake, fake, 200, 128, 64, fake, 16, None) == WS_SMALL
 
 
 def test_static_scratch_entry_checks_launch_nothing(lib):

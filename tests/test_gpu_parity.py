@@ -124,7 +124,7 @@ def test_gemm_small_full_parity(oracle_mod, M, N, K):
     bq, bs, W = quantized_weight(oracle_mod, B)
     aq, as_, c64, c16 = oracle_mod.quant_gemm(A, bq, bs)
     Ad = A.cuda()
-    C_fused = mx.quant_gemm(Ad, W)  # two-pass route for M >= 64 (workspace from torch)
+    C_fused = mx.quant_gemm(Ad, W)  # the library's route (a workspace from torch when it asks for one)
     no_ws = torch.empty(0, dtype=torch.uint8, device="cuda")
     C_single = mx.quant_gemm(Ad, W, workspace=no_ws)  # always the single fused kernel
     Aq, As = mx.quantize(Ad)
