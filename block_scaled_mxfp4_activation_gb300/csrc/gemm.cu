@@ -1187,18 +1187,17 @@ static int active_clusters(const mxfp4_plan_t& p, bool fused) {
 // a split runs in sequence costs ~250 ns (operand loads, tensor-memory scale
 // copies, four MMAs) plus, on the fused kernel, ~200 ns per 32 activation rows
 // it quantizes (so 16-row tiles halve it: at M = 32 two CTAs of 16 rows beat
-// one of 32); a K split adds ~700 ns for the reduction; a split with more K
-// tiles than stages adds ~1 us per reload, divided by the stages in flight
-// (measured on GB300 with graph-replayed calls).  Among plans that run in one
-// wave, those that leave room for the next call's CTAs beside this call's
-// (twice the CTAs fit at the plan's CTAs per SM) come first: the next call
-// then starts early under programmatic launch, and losing that overlap costs
-// more than a deeper stage ring gains (K = 7168, 7 splits: 2 stages 5.6 us,
-// 4 stages with one CTA per SM 10.0 us).  Candidates: block_m from the
-// smallest tile that holds M (capped at 128) down to a quarter of it; every
-// split count that leaves no split empty; 1 to 6 stages (at most the split's
-// K tiles).  Ties prefer the larger block_m (fewer re-reads of the weights),
-// then the larger stage count, then fewer splits.
+// one of 32); a K split adds ~700 ns + 10 ns per row for the reduction; a
+// split with more K tiles than stages adds ~1 us per reload, divided by the
+// stages in flight; and a plan whose CTAs leave no room for the next call's
+// beside them (twice the CTAs do not fit at the plan's CTAs per SM) adds
+// ~0.5 us, the overlap the next call loses under programmatic launch
+// (measured on GB300 with graph-replayed calls).  Candidates: block_m from the
+// smallest tile that holds M (capped at 128; at 32 on the fused kernel up to
+// M = 128) down to a quarter of it; every split count that leaves no split
+// empty; 1 to 6 stages (at most the split's K tiles).  Ties prefer the larger
+// block_m (fewer re-reads of the weights), then the larger stage count, then
+// fewer splits.
 // Plans measured best on GB300 (152 SMs) for shapes of the leaderboard where
 // the estimate is not (keyed on the shape): sweeps of block_m x splits x
 // stages x share, graph-replayed calls with rotating operands.  `fused` is the
@@ -1276,7 +1275,9 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
   if (fused && M <= 128 && bm0 > 32) bm0 = 32;
   const int64_t k_tiles = ceil_div(K, kTileK);
   const int64_t cap = 2 * static_cast<int64_t>(prop.multiProcessorCount);
-  int64_t best[6] = {-1, 0, 0, 0, 0, 0};
+  // score: one wave, then the estimate (or fewer CTAs), block_m, stages, fewer splits
+  constexpr int kScore = 5;
+  int64_t best[kScore] = {-1, 0, 0, 0, 0};
   for (int bm = bm0; bm >= 16 && bm * 4 >= bm0; bm /= 2) {
     for (int64_t splits = 1; splits <= kMaxSplits && splits <= k_tiles; ++splits) {
       const int64_t per = ceil_div(k_tiles, splits);
@@ -1301,16 +1302,16 @@ void default_plan(int64_t M, int64_t N, int64_t K, bool fused, const cudaDeviceP
         // estimates: 256x2880x7168 12.6 us with 2 splits against 16.8 without)
         const bool room_for_next = 2 * ctas <= per_sm * static_cast<int64_t>(prop.multiProcessorCount);
         const int64_t cost = plan_cost_ns(q, M, fused) + (room_for_next ? 0 : kNoRoomNs);
-        const int64_t score[6] = {one_wave, 0, one_wave ? -cost : -ctas, bm, st, -splits};
+        const int64_t score[kScore] = {one_wave, one_wave ? -cost : -ctas, bm, st, -splits};
         bool better = false;
-        for (int i = 0; i < 6; ++i) {
+        for (int i = 0; i < kScore; ++i) {
           if (score[i] != best[i]) {
             better = score[i] > best[i];
             break;
           }
         }
         if (better) {
-          for (int i = 0; i < 6; ++i) best[i] = score[i];
+          for (int i = 0; i < kScore; ++i) best[i] = score[i];
           *p = q;
         }
       }
